@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""Benchmark of the Groth16 quotient-evaluation (H) path over BN254 Fr on GB300.
+
+One step = one whole H computation (gather, three inverse NTTs with 1/n, coset shift,
+three forward NTTs, join in both encodings) on the proving-key-shaped 2^18 workload
+(140296 constraints, 262144 wires, CSR A/B with the GATHER_CU page's row statistics),
+inputs resident in HBM. The working set (~90 MB) fits in L2, so L2 is flushed (a
+256 MiB write) between timed steps, outside the timed events.
+
+Prints ONE JSON line. Under torchrun every rank runs its own replica (independent
+proofs, no data exchange); value = steps x ranks / max-over-ranks time.
+
+--impl reference times the CPU oracle (plain C, one thread) on the same workload: the
+only reference implementation this path has.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Groth16 H computations/s at 2^18"
+UNIT = "H/s"
+LOG_N = 18
+WORKLOAD = "groth16_h_bn254_2^18"
+# IMAD-class operations per Montgomery multiply (64 + 64 wide 32x32 products, 8 low
+# products) and per Montgomery reduction (from_mont).
+OPS_PER_MM = 136
+OPS_PER_FROM_MONT = 72
+SM_COUNT = 152
+IMAD_PER_CLK_PER_SM = 64
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extra", action="store_true", help="skip the 2^22 secondary lines")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def plan_for(k):
+    """Slice levels of the launch plan (mirrors the library): (kk per level)."""
+    if k <= 22:
+        lo = (k + 1) // 2
+        return [lo, k - lo]
+    lo = (k + 2) // 3
+    rest = k - lo
+    mid = (rest + 1) // 2
+    return [lo, mid, rest - mid]
+
+
+def algorithmic_ops(kernel, k, nnz_a, nnz_b):
+    """Algorithmic IMAD-class operations of one launch, from the method's multiply count
+    per H: 6 (n/2) k butterfly multiplies, 3n for 1/n, 3n for the shift, n for the join
+    product, nnz_A + nnz_B + n for the gather, and n Montgomery reductions for h_std."""
+    n = 1 << k
+    kk = plan_for(k)
+    if kernel == "gather":
+        return OPS_PER_MM * (nnz_a + nnz_b + n)
+    if kernel == "ntt_dif":
+        return OPS_PER_MM * 3 * kk[-1] * (n // 2)
+    if kernel == "ntt_mid":
+        return OPS_PER_MM * 3 * (kk[0] * n + 2 * n)
+    if kernel == "ntt_dit_join":
+        return OPS_PER_MM * (3 * kk[-1] * (n // 2) + n) + OPS_PER_FROM_MONT * n
+    if kernel == "ntt_dit":
+        return OPS_PER_MM * 3 * kk[1] * (n // 2)
+    return 0
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.monotonic(), float(parts[0]), float(parts[1]),
+                                     parts[3:7]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside
+        if not used and self.samples:  # region shorter than the sampling period
+            used = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({self.NAMES[i] for s in used for i, v in enumerate(s[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(s[1] for s in used),
+                "sm_max_mhz": max(s[2] for s in used), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def cpu_baseline(A, B, w, budget_s=12.0, max_runs=20):
+    """The oracle as it stands, one thread, on whole 2^18 H computations."""
+    import oracle
+
+    oracle.build()
+    runs, total = 0, 0.0
+    while runs < max_runs and (total < budget_s or runs == 0):
+        t = time.perf_counter()
+        oracle.compute_h(LOG_N, A, B, w)
+        total += time.perf_counter() - t
+        runs += 1
+    return {"value": runs / total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d whole 2^18 H computations (%.1f s), C oracle, one thread" % (
+                runs, total)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from bn254_scalar_field_gb300 import synth
+    import oracle
+
+    oracle.build()
+    A, B, w = synth.problem(LOG_N)
+    for _ in range(args.warmup):
+        oracle.compute_h(LOG_N, A, B, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.compute_h(LOG_N, A, B, w)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "impl": "CPU oracle (plain C, 4x64-bit limbs)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d whole 2^18 H computations, one thread" % args.steps},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+
+    from bn254_scalar_field_gb300 import build, g3h, synth
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    build.build()
+    dev = torch.device("cuda", local)
+    n = 1 << LOG_N
+    A, B, w = synth.problem(LOG_N)
+    nnz_a, nnz_b = int(A[0][-1]), int(B[0][-1])
+    ctx = g3h.Context(LOG_N, w.shape[0], A, B, device=local)
+    wd = torch.from_numpy(w.view(np.int32)).to(dev)
+    hm = torch.empty((n, 8), dtype=torch.int32, device=dev)
+    hs = torch.empty((n, 8), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        ctx.compute_h(wd, hm, hs)
+        flush.fill_(1)
+    ctx.sync()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    time.sleep(0.1)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ctx.timing_enable(True)
+    t0 = time.monotonic()
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        ctx.compute_h(wd, hm, hs)
+        evs[i][1].record(stream)
+        flush.fill_(i & 0xFF)
+    torch.cuda.synchronize(dev)
+    t1 = time.monotonic()
+    if dist:
+        dist.barrier()
+    ctx.sync()
+    kt = ctx.timing_read()
+    ctx.timing_enable(False)
+    sampler.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if dist:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * args.steps / (step_ms / 1e3)
+    launches = sum(v[0] for v in kt.values())
+
+    # roofline of the dominant kernel: algorithmic IMAD-class ops per launch / mean time
+    top = max(kt, key=lambda k: kt[k][1])
+    top_launches, top_ms = kt[top]
+    per_launch_ms = top_ms / top_launches
+    ops = algorithmic_ops(top, LOG_N, nnz_a, nnz_b)
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    peak_tops = SM_COUNT * IMAD_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+    achieved = ops / (per_launch_ms * 1e-3) / 1e12
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+        from bn254_scalar_field_gb300.build import source_digest
+
+        ent = rec.get(top)
+        if ent and ent.get("source_digest") == source_digest() and ent.get("log_n") == LOG_N:
+            traffic = ent["bytes_per_launch"]
+    except (OSError, ValueError, ImportError):
+        pass
+    per_h_ops = sum(algorithmic_ops(k, LOG_N, nnz_a, nnz_b) * v[0] for k, v in kt.items())
+    per_h_ops /= args.steps
+    roofline = {
+        "bound": "alu", "kernel": top, "achieved": achieved, "peak": peak_tops,
+        "unit": "T IMAD-ops/s", "frac": achieved / peak_tops, "traffic": traffic,
+        "peak_source": "derived: %d SMs x %d 32-bit IMAD/clk/SM x %.0f MHz" % (
+            SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
+        "whole_step_frac": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / peak_tops,
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()},
+    }
+
+    # end to end through the public API with host (pinned) buffers, copies included
+    wp = torch.from_numpy(w.view(np.int32)).pin_memory()
+    hmp = torch.empty((n, 8), dtype=torch.int32).pin_memory()
+    hsp = torch.empty((n, 8), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        ctx.compute_h(wp, hmp, hsp)
+    e2e_s = 0.0
+    for _ in range(e2e_steps):
+        flush.fill_(3)
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        ctx.compute_h(wp, hmp, hsp)
+        e2e_s += time.perf_counter() - t
+    if dist:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
+           "h2d_bytes_per_step": int(w.nbytes), "d2h_bytes_per_step": int(2 * n * 32)}
+
+    extra = {"ntt_gelem_s_2^18_in_h": 6 * n / (step_ms / args.steps * 1e-3) / 1e9}
+    if not args.no_extra and rank == 0:
+        extra.update(stress_2_22(torch, dev, g3h, synth))
+    ctx.close()
+
+    if rank == 0:
+        cpu = None if args.no_cpu else cpu_baseline(A, B, w)
+        clocks = sampler.summary(t0, t1)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "constraints": 140296, "wires": int(w.shape[0]),
+                       "nnz_a": nnz_a, "nnz_b": nnz_b, "parallelism": "replicas x%d" % world,
+                       "l2": "flushed between timed steps (256 MiB write)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "extra": extra,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def stress_2_22(torch, dev, g3h, synth):
+    """Secondary figures on the 2^22 stress vectors (inputs larger than L2): one forward
+    coset NTT (Fr NTT Gelem/s) and the H path on given a, b, c = a*b."""
+    k = synth.STRESS_LOG_N
+    n = 1 << k
+    a, b = synth.stress_ab(k)
+    ctx = g3h.Context(k, device=dev.index)
+    ad = torch.from_numpy(a.view(np.int32)).to(dev)
+    bd = torch.from_numpy(b.view(np.int32)).to(dev)
+    cd = torch.empty_like(ad)
+    ctx.mul(ad, bd, cd)
+    hm = torch.empty_like(ad)
+    hs = torch.empty_like(ad)
+    x = ad.clone()
+    stream = torch.cuda.current_stream(dev)
+    reps = 10
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    ntt_ms = timed(lambda: ctx.ntt(x, coset=True))
+    h_ms = timed(lambda: ctx.compute_h_abc(ad, bd, cd, hm, hs))
+    ctx.sync()
+    ctx.close()
+    return {"ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,
+            "h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
+            "ntt_gelem_s_2^22_in_h": 6 * n / (h_ms * 1e-3) / 1e9}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,263 @@
+// BN254 scalar field Fr on sm_103a: 8 x 32-bit little-endian limbs, Montgomery form
+// with R = 2^256.
+//
+// The field is the one the "snarkrs_gpu_kernels" pages compute in (POINTWISE_CU, "two
+// output buffers": Montgomery limbs vs the integer in [0, r)); its modulus is
+//   r = 0x30644e72e131a029b85045b68181585d2833e84879b9709143e1f593f0000001.
+// The arithmetic here is written from the mathematics, not from any header the pages
+// mention: Montgomery multiplication in coarsely integrated operand scanning (CIOS) form
+// (Koc, Acar & Kaliski, "Analyzing and Comparing Montgomery Multiplication Algorithms",
+// IEEE Micro 1996) on 32-bit words, and additions and subtractions as PTX add-with-carry
+// chains.
+//
+// Lazy reduction. 4r < 2^256, so every intermediate value is kept in [0, 2r):
+//   * fr_mul with both inputs in [0, 2r) returns a value in [0, 2r) without the final
+//     conditional subtraction, because (a*b + m*r) / R < (4r^2 + R*r) / R < 2r;
+//   * fr_add / fr_sub fold their result back into [0, 2r) with one conditional 2r;
+//   * fr_canon maps [0, 2r) to the canonical [0, r). Every value that leaves the library
+//     goes through it.
+#pragma once
+#include <stdint.h>
+
+namespace g3h {
+
+struct __align__(16) fr_t {
+  uint32_t v[8];
+};
+
+// r, 2r and -r^{-1} mod 2^32.
+#define G3H_R0 0xf0000001u
+#define G3H_R1 0x43e1f593u
+#define G3H_R2 0x79b97091u
+#define G3H_R3 0x2833e848u
+#define G3H_R4 0x8181585du
+#define G3H_R5 0xb85045b6u
+#define G3H_R6 0xe131a029u
+#define G3H_R7 0x30644e72u
+
+#define G3H_2R0 0xe0000002u
+#define G3H_2R1 0x87c3eb27u
+#define G3H_2R2 0xf372e122u
+#define G3H_2R3 0x5067d090u
+#define G3H_2R4 0x0302b0bau
+#define G3H_2R5 0x70a08b6du
+#define G3H_2R6 0xc2634053u
+#define G3H_2R7 0x60c89ce5u
+
+#define G3H_NPRIME 0xefffffffu
+
+__device__ __forceinline__ fr_t fr_zero() {
+  fr_t z;
+#pragma unroll
+  for (int i = 0; i < 8; i++) z.v[i] = 0u;
+  return z;
+}
+
+// a * b * 2^-256 mod r, inputs in [0, 2r), output in [0, 2r).
+//
+// CIOS: for each word b_i of b, t <- (t + a * b_i + m * r) / 2^32 with
+// m = (t + a*b_i) * (-r^{-1}) mod 2^32. Each step of the inner loops is a 32x32 -> 64
+// multiply plus two 32-bit addends, (2^32-1)^2 + 2(2^32-1) = 2^64 - 1, so it never
+// overflows 64 bits; written with 64-bit products the compiler issues wide multiply-adds
+// (measured faster on this GPU than separate low/high multiply chains). On entry to a
+// row t < 3r < 2^256, so t fits eight words plus the carry word t8 of the row.
+__device__ __forceinline__ fr_t fr_mul(const fr_t& a, const fr_t& b) {
+  const uint32_t R[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
+  uint32_t t[9];
+#pragma unroll
+  for (int j = 0; j < 9; j++) t[j] = 0;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    uint64_t c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      uint64_t s = (uint64_t)a.v[j] * b.v[i] + t[j] + c;
+      t[j] = (uint32_t)s;
+      c = s >> 32;
+    }
+    t[8] = (uint32_t)c;
+    uint32_t m = t[0] * G3H_NPRIME;
+    uint64_t s = (uint64_t)m * R[0] + t[0];
+    c = s >> 32;
+#pragma unroll
+    for (int j = 1; j < 8; j++) {
+      s = (uint64_t)m * R[j] + t[j] + c;
+      t[j - 1] = (uint32_t)s;
+      c = s >> 32;
+    }
+    t[7] = t[8] + (uint32_t)c;
+  }
+  fr_t r;
+#pragma unroll
+  for (int j = 0; j < 8; j++) r.v[j] = t[j];
+  return r;
+}
+
+// a + b, inputs in [0, 2r), output in [0, 2r): the sum is below 4r < 2^256, and 2r is
+// subtracted when the subtraction does not borrow.
+__device__ __forceinline__ fr_t fr_add(const fr_t& a, const fr_t& b) {
+  fr_t s, d;
+  uint32_t borrow;
+  asm("add.cc.u32  %0, %8,  %16;\n\t"
+      "addc.cc.u32 %1, %9,  %17;\n\t"
+      "addc.cc.u32 %2, %10, %18;\n\t"
+      "addc.cc.u32 %3, %11, %19;\n\t"
+      "addc.cc.u32 %4, %12, %20;\n\t"
+      "addc.cc.u32 %5, %13, %21;\n\t"
+      "addc.cc.u32 %6, %14, %22;\n\t"
+      "addc.u32    %7, %15, %23;"
+      : "=r"(s.v[0]), "=r"(s.v[1]), "=r"(s.v[2]), "=r"(s.v[3]), "=r"(s.v[4]), "=r"(s.v[5]),
+        "=r"(s.v[6]), "=r"(s.v[7])
+      : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]),
+        "r"(a.v[6]), "r"(a.v[7]), "r"(b.v[0]), "r"(b.v[1]), "r"(b.v[2]), "r"(b.v[3]),
+        "r"(b.v[4]), "r"(b.v[5]), "r"(b.v[6]), "r"(b.v[7]));
+  asm("sub.cc.u32  %0, %9,  0xe0000002;\n\t"
+      "subc.cc.u32 %1, %10, 0x87c3eb27;\n\t"
+      "subc.cc.u32 %2, %11, 0xf372e122;\n\t"
+      "subc.cc.u32 %3, %12, 0x5067d090;\n\t"
+      "subc.cc.u32 %4, %13, 0x0302b0ba;\n\t"
+      "subc.cc.u32 %5, %14, 0x70a08b6d;\n\t"
+      "subc.cc.u32 %6, %15, 0xc2634053;\n\t"
+      "subc.cc.u32 %7, %16, 0x60c89ce5;\n\t"
+      "subc.u32    %8, 0, 0;"
+      : "=r"(d.v[0]), "=r"(d.v[1]), "=r"(d.v[2]), "=r"(d.v[3]), "=r"(d.v[4]), "=r"(d.v[5]),
+        "=r"(d.v[6]), "=r"(d.v[7]), "=r"(borrow)
+      : "r"(s.v[0]), "r"(s.v[1]), "r"(s.v[2]), "r"(s.v[3]), "r"(s.v[4]), "r"(s.v[5]),
+        "r"(s.v[6]), "r"(s.v[7]));
+  // borrow is 0xffffffff when s < 2r, 0 otherwise.
+#pragma unroll
+  for (int i = 0; i < 8; i++) d.v[i] = borrow ? s.v[i] : d.v[i];
+  return d;
+}
+
+// a - b, inputs in [0, 2r), output in [0, 2r): 2r is added back when the difference
+// borrows.
+__device__ __forceinline__ fr_t fr_sub(const fr_t& a, const fr_t& b) {
+  fr_t d;
+  uint32_t borrow;
+  asm("sub.cc.u32  %0, %9,  %17;\n\t"
+      "subc.cc.u32 %1, %10, %18;\n\t"
+      "subc.cc.u32 %2, %11, %19;\n\t"
+      "subc.cc.u32 %3, %12, %20;\n\t"
+      "subc.cc.u32 %4, %13, %21;\n\t"
+      "subc.cc.u32 %5, %14, %22;\n\t"
+      "subc.cc.u32 %6, %15, %23;\n\t"
+      "subc.cc.u32 %7, %16, %24;\n\t"
+      "subc.u32    %8, 0, 0;"
+      : "=r"(d.v[0]), "=r"(d.v[1]), "=r"(d.v[2]), "=r"(d.v[3]), "=r"(d.v[4]), "=r"(d.v[5]),
+        "=r"(d.v[6]), "=r"(d.v[7]), "=r"(borrow)
+      : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]),
+        "r"(a.v[6]), "r"(a.v[7]), "r"(b.v[0]), "r"(b.v[1]), "r"(b.v[2]), "r"(b.v[3]),
+        "r"(b.v[4]), "r"(b.v[5]), "r"(b.v[6]), "r"(b.v[7]));
+  asm("add.cc.u32  %0, %0, %8;\n\t"
+      "addc.cc.u32 %1, %1, %9;\n\t"
+      "addc.cc.u32 %2, %2, %10;\n\t"
+      "addc.cc.u32 %3, %3, %11;\n\t"
+      "addc.cc.u32 %4, %4, %12;\n\t"
+      "addc.cc.u32 %5, %5, %13;\n\t"
+      "addc.cc.u32 %6, %6, %14;\n\t"
+      "addc.u32    %7, %7, %15;"
+      : "+r"(d.v[0]), "+r"(d.v[1]), "+r"(d.v[2]), "+r"(d.v[3]), "+r"(d.v[4]), "+r"(d.v[5]),
+        "+r"(d.v[6]), "+r"(d.v[7])
+      : "r"(borrow & G3H_2R0), "r"(borrow & G3H_2R1), "r"(borrow & G3H_2R2),
+        "r"(borrow & G3H_2R3), "r"(borrow & G3H_2R4), "r"(borrow & G3H_2R5),
+        "r"(borrow & G3H_2R6), "r"(borrow & G3H_2R7));
+  return d;
+}
+
+// [0, 2r) -> [0, r).
+__device__ __forceinline__ fr_t fr_canon(const fr_t& a) {
+  fr_t d;
+  uint32_t borrow;
+  asm("sub.cc.u32  %0, %9,  0xf0000001;\n\t"
+      "subc.cc.u32 %1, %10, 0x43e1f593;\n\t"
+      "subc.cc.u32 %2, %11, 0x79b97091;\n\t"
+      "subc.cc.u32 %3, %12, 0x2833e848;\n\t"
+      "subc.cc.u32 %4, %13, 0x8181585d;\n\t"
+      "subc.cc.u32 %5, %14, 0xb85045b6;\n\t"
+      "subc.cc.u32 %6, %15, 0xe131a029;\n\t"
+      "subc.cc.u32 %7, %16, 0x30644e72;\n\t"
+      "subc.u32    %8, 0, 0;"
+      : "=r"(d.v[0]), "=r"(d.v[1]), "=r"(d.v[2]), "=r"(d.v[3]), "=r"(d.v[4]), "=r"(d.v[5]),
+        "=r"(d.v[6]), "=r"(d.v[7]), "=r"(borrow)
+      : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]),
+        "r"(a.v[6]), "r"(a.v[7]));
+#pragma unroll
+  for (int i = 0; i < 8; i++) d.v[i] = borrow ? a.v[i] : d.v[i];
+  return d;
+}
+
+// Montgomery reduction of a canonical value: a * 2^-256 mod r, i.e. the standard-form
+// integer of a Montgomery representative. For a < r the result (a + M*r) / R is below r,
+// so it is canonical with no final subtraction.
+__device__ __forceinline__ fr_t fr_from_mont(const fr_t& a) {
+  const uint32_t R[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
+  uint32_t t[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) t[j] = a.v[j];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    uint32_t m = t[0] * G3H_NPRIME;
+    uint64_t s = (uint64_t)m * R[0] + t[0];
+    uint64_t c = s >> 32;
+#pragma unroll
+    for (int j = 1; j < 8; j++) {
+      s = (uint64_t)m * R[j] + t[j] + c;
+      t[j - 1] = (uint32_t)s;
+      c = s >> 32;
+    }
+    t[7] = (uint32_t)c;
+  }
+  fr_t r;
+#pragma unroll
+  for (int j = 0; j < 8; j++) r.v[j] = t[j];
+  return r;
+}
+
+// True when a < r (the canonical range every input must be in).
+__device__ __forceinline__ bool fr_is_canonical(const fr_t& a) {
+  uint32_t borrow;
+  asm("{\n\t"
+      ".reg .u32 x;\n\t"
+      "sub.cc.u32  x, %1, 0xf0000001;\n\t"
+      "subc.cc.u32 x, %2, 0x43e1f593;\n\t"
+      "subc.cc.u32 x, %3, 0x79b97091;\n\t"
+      "subc.cc.u32 x, %4, 0x2833e848;\n\t"
+      "subc.cc.u32 x, %5, 0x8181585d;\n\t"
+      "subc.cc.u32 x, %6, 0xb85045b6;\n\t"
+      "subc.cc.u32 x, %7, 0xe131a029;\n\t"
+      "subc.cc.u32 x, %8, 0x30644e72;\n\t"
+      "subc.u32    %0, 0, 0;\n\t"
+      "}"
+      : "=r"(borrow)
+      : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]),
+        "r"(a.v[6]), "r"(a.v[7]));
+  return borrow != 0u;
+}
+
+// 32-byte loads and stores as two 16-byte vector accesses.
+__device__ __forceinline__ fr_t fr_load(const fr_t* p) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 x = q[0], y = q[1];
+  fr_t a;
+  a.v[0] = x.x; a.v[1] = x.y; a.v[2] = x.z; a.v[3] = x.w;
+  a.v[4] = y.x; a.v[5] = y.y; a.v[6] = y.z; a.v[7] = y.w;
+  return a;
+}
+
+__device__ __forceinline__ fr_t fr_ldg(const fr_t* p) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 x = __ldg(q), y = __ldg(q + 1);
+  fr_t a;
+  a.v[0] = x.x; a.v[1] = x.y; a.v[2] = x.z; a.v[3] = x.w;
+  a.v[4] = y.x; a.v[5] = y.y; a.v[6] = y.z; a.v[7] = y.w;
+  return a;
+}
+
+__device__ __forceinline__ void fr_store(fr_t* p, const fr_t& a) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+  q[0] = make_uint4(a.v[0], a.v[1], a.v[2], a.v[3]);
+  q[1] = make_uint4(a.v[4], a.v[5], a.v[6], a.v[7]);
+}
+
+}  // namespace g3h

@@ -1,0 +1,679 @@
+// The C ABI of include/g3h.h: context, resident tables, launch plans.
+//
+// Work per H computation on a domain of 2^k >= 2^6 points (two slice levels, k = lo + hi;
+// three levels for k > 22; a slice is at most 2^11 elements):
+//   k_gather                 a, b, c                       (skipped by compute_h_abc)
+//   k_ntt_dif  (3 vectors)   inverse passes on the top bits, strided slices
+//   k_ntt_mid  (3 vectors)   inverse passes on the low bits, shift g^brev(p)/n, forward
+//                            passes on the low bits, contiguous slices
+//   k_ntt_dit  (join)        forward passes on the top bits for a, b, then c with
+//                            h = a*b - c written in both encodings at c's store
+// All launches go to the context's stream in order; nothing synchronises between them.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/g3h.h"
+#include "kernels.cuh"
+
+using namespace g3h;
+
+namespace {
+
+const uint32_t kModulus[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
+
+bool host_canonical(const uint32_t* x) {
+  for (int i = 7; i >= 0; i--) {
+    if (x[i] < kModulus[i]) return true;
+    if (x[i] > kModulus[i]) return false;
+  }
+  return false;  // equal to r
+}
+
+struct TimedLaunch {
+  const char* name;
+  cudaEvent_t e0, e1;
+};
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+// Slice levels of a transform of 2^k points: level 0 is the contiguous low slice.
+struct Plan {
+  int levels;
+  uint32_t kk[3];
+  uint32_t c0[3];
+};
+
+Plan plan_for(uint32_t k) {
+  Plan p{};
+  if (k <= 22) {
+    const uint32_t lo = (k + 1) / 2;
+    p.levels = 2;
+    p.kk[0] = lo;
+    p.kk[1] = k - lo;
+    p.c0[0] = 0;
+    p.c0[1] = lo;
+  } else {
+    const uint32_t lo = (k + 2) / 3, rest = k - lo, mid = (rest + 1) / 2;
+    p.levels = 3;
+    p.kk[0] = lo;
+    p.kk[1] = mid;
+    p.kk[2] = rest - mid;
+    p.c0[0] = 0;
+    p.c0[1] = lo;
+    p.c0[2] = lo + mid;
+  }
+  return p;
+}
+
+}  // namespace
+
+struct g3h_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  uint32_t log_n = 0, n_wires = 0;
+  size_t n = 0;
+  bool has_csr = false;
+  uint32_t n_rows_a = 0, n_rows_b = 0;
+  uint32_t *d_rpa = nullptr, *d_cola = nullptr, *d_rpb = nullptr, *d_colb = nullptr;
+  fr_t *d_vala = nullptr, *d_valb = nullptr;
+  fr_t* d_consts = nullptr;  // omega, omega^-1, g, g^-1, n^-1, 1 (Montgomery)
+  fr_t *d_tw_fwd = nullptr, *d_tw_inv = nullptr, *d_shift_br = nullptr;
+  fr_t *d_coset_fwd = nullptr, *d_coset_inv = nullptr;
+  fr_t* d_abc = nullptr;  // 3n scratch
+  fr_t* d_stage = nullptr;
+  size_t stage_elems = 0;
+  uint32_t* d_err = nullptr;
+  fr_t h_consts[6];
+  bool timing = false;
+  std::vector<TimedLaunch> launches;
+  std::vector<cudaEvent_t> event_pool;
+  size_t events_used = 0;
+};
+
+namespace {
+
+template <class T>
+int dalloc(T** p, size_t count) {
+  if (count == 0) count = 1;
+  return cudaMalloc((void**)p, count * sizeof(T)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+}
+
+void release(g3h_ctx* c) {
+  void* bufs[] = {c->d_rpa,      c->d_cola,     c->d_rpb,      c->d_colb,        c->d_vala,
+                  c->d_valb,     c->d_consts,   c->d_tw_fwd,   c->d_tw_inv,      c->d_shift_br,
+                  c->d_coset_fwd, c->d_coset_inv, c->d_abc,    c->d_stage,       c->d_err};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+}
+
+cudaEvent_t take_event(g3h_ctx* c) {
+  if (c->events_used == c->event_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    c->event_pool.push_back(e);
+  }
+  return c->event_pool[c->events_used++];
+}
+
+template <class F>
+int run(g3h_ctx* c, const char* name, F&& launch) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (c->timing) {
+    e0 = take_event(c);
+    e1 = take_event(c);
+    if (e0 && e1) cudaEventRecord(e0, c->stream);
+  }
+  launch();
+  const cudaError_t err = cudaGetLastError();
+  if (c->timing && e0 && e1) {
+    cudaEventRecord(e1, c->stream);
+    c->launches.push_back({name, e0, e1});
+  }
+  return err == cudaSuccess ? G3H_OK : G3H_E_CUDA;
+}
+
+unsigned blocks_for(size_t count, unsigned per) { return (unsigned)((count + per - 1) / per); }
+
+int launch_slice(g3h_ctx* c, const char* name, void (*kern)(SliceArgs), const SliceArgs& a,
+                 unsigned nvec) {
+  const dim3 grid((unsigned)(c->n >> a.kk), nvec);
+  const dim3 block(1u << (a.kk - 3u));
+  const size_t smem = (size_t)32 << a.kk;
+  return run(c, name, [&] { kern<<<grid, block, smem, c->stream>>>(a); });
+}
+
+int set_smem_limits() {
+  const int bytes = 32 << 11;  // the largest slice, 2^11 elements
+  void (*kerns[])(SliceArgs) = {k_ntt_dif, k_ntt_mid, k_ntt_dit, k_ntt_brev};
+  for (auto k : kerns)
+    if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return G3H_E_CUDA;
+  return G3H_OK;
+}
+
+int build_table(g3h_ctx* c, fr_t* tab, size_t count, int base, int scale, uint32_t brev) {
+  if (count == 0) return G3H_OK;
+  return run(c, "tables", [&] {
+    k_pow_table<<<blocks_for(count, 256), 256, 0, c->stream>>>(tab, count, c->d_consts, base,
+                                                                scale, brev);
+  });
+}
+
+int ensure_coset_tables(g3h_ctx* c) {
+  if (c->d_coset_fwd) return G3H_OK;
+  int rc = dalloc(&c->d_coset_fwd, c->n);
+  if (rc == G3H_OK) rc = dalloc(&c->d_coset_inv, c->n);
+  if (rc != G3H_OK) return rc;
+  rc = build_table(c, c->d_coset_fwd, c->n, 2, -1, 0);
+  if (rc == G3H_OK) rc = build_table(c, c->d_coset_inv, c->n, 3, 4, 0);
+  return rc;
+}
+
+int ensure_stage(g3h_ctx* c, size_t elems) {
+  if (c->stage_elems >= elems) return G3H_OK;
+  if (c->d_stage) cudaFree(c->d_stage);
+  c->d_stage = nullptr;
+  c->stage_elems = 0;
+  if (dalloc(&c->d_stage, elems) != G3H_OK) return G3H_E_NOMEM;
+  c->stage_elems = elems;
+  return G3H_OK;
+}
+
+int h2d(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
+  if (bytes == 0) return G3H_OK;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, c->stream) == cudaSuccess
+             ? G3H_OK
+             : G3H_E_CUDA;
+}
+
+int d2h(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
+  if (bytes == 0) return G3H_OK;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, c->stream) == cudaSuccess
+             ? G3H_OK
+             : G3H_E_CUDA;
+}
+
+// Waits for the stream and reports (then clears) the device-side input check word.
+int finish(g3h_ctx* c) {
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
+  uint32_t err = 0;
+  if (cudaMemcpy(&err, c->d_err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return G3H_E_CUDA;
+  if (err) {
+    if (cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess) return G3H_E_CUDA;
+    return G3H_E_NONCANON;
+  }
+  return G3H_OK;
+}
+
+SliceArgs base_args(g3h_ctx* c, uint32_t flags) {
+  SliceArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.err = c->d_err;
+  a.log_n = c->log_n;
+  (void)flags;
+  return a;
+}
+
+// Steps 2-5 on device vectors a, b, c -> h_mont, h_std (device). a, b, c may be the
+// context's scratch vectors.
+int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, fr_t* hm, fr_t* hs,
+             uint32_t flags) {
+  const uint32_t k = c->log_n;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  const size_t n = c->n;
+  if (k <= kSmallMaxLog) {
+    return run(c, "small_quotient", [&] {
+      k_small_quotient<<<1, 32, 0, c->stream>>>(a, b, cc, c->d_tw_inv, c->d_tw_fwd,
+                                                 c->d_shift_br, hm, hs, k, check, c->d_err);
+    });
+  }
+  fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
+  const Plan pl = plan_for(k);
+  int rc = G3H_OK;
+  // inverse, top levels first
+  for (int lvl = pl.levels - 1; lvl >= 1 && rc == G3H_OK; lvl--) {
+    SliceArgs x = base_args(c, flags);
+    const bool first = lvl == pl.levels - 1;
+    x.src[0] = first ? a : s[0];
+    x.src[1] = first ? b : s[1];
+    x.src[2] = first ? cc : s[2];
+    for (int v = 0; v < 3; v++) x.dst[v] = s[v];
+    x.tw = c->d_tw_inv;
+    x.kk = pl.kk[lvl];
+    x.c0 = pl.c0[lvl];
+    x.mode = (first && check) ? SL_CHECK : 0u;
+    rc = launch_slice(c, "ntt_dif", k_ntt_dif, x, 3);
+  }
+  if (rc != G3H_OK) return rc;
+  {
+    SliceArgs x = base_args(c, flags);
+    for (int v = 0; v < 3; v++) x.dst[v] = s[v];
+    x.tw = c->d_tw_inv;
+    x.tw2 = c->d_tw_fwd;
+    x.scale_tab = c->d_shift_br;
+    x.kk = pl.kk[0];
+    x.c0 = 0;
+    rc = launch_slice(c, "ntt_mid", k_ntt_mid, x, 3);
+  }
+  // forward, middle levels
+  for (int lvl = 1; lvl < pl.levels - 1 && rc == G3H_OK; lvl++) {
+    SliceArgs x = base_args(c, flags);
+    for (int v = 0; v < 3; v++) x.src[v] = x.dst[v] = s[v];
+    x.tw = c->d_tw_fwd;
+    x.kk = pl.kk[lvl];
+    x.c0 = pl.c0[lvl];
+    rc = launch_slice(c, "ntt_dit", k_ntt_dit, x, 3);
+  }
+  if (rc != G3H_OK) return rc;
+  const int top = pl.levels - 1;
+  SliceArgs x = base_args(c, flags);
+  for (int v = 0; v < 3; v++) x.src[v] = x.dst[v] = s[v];
+  x.tw = c->d_tw_fwd;
+  x.kk = pl.kk[top];
+  x.c0 = pl.c0[top];
+  if (!(flags & G3H_UNFUSED_JOIN)) {
+    x.mode = SL_JOIN;
+    x.h_mont = hm;
+    x.h_std = hs;
+    return launch_slice(c, "ntt_dit_join", k_ntt_dit, x, 1);
+  }
+  rc = launch_slice(c, "ntt_dit", k_ntt_dit, x, 3);
+  if (rc != G3H_OK) return rc;
+  return run(c, "join", [&] {
+    k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
+  });
+}
+
+int gather(g3h_ctx* c, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc, uint32_t flags) {
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  const uint32_t n = (uint32_t)c->n;
+  return run(c, "gather", [&] {
+    k_gather<<<blocks_for(n, 256), 256, 0, c->stream>>>(
+        c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
+        c->n_rows_b, n, a, b, cc, check, c->d_err);
+  });
+}
+
+int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
+  const uint32_t k = c->log_n;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  if (coset) {
+    const int rc = ensure_coset_tables(c);
+    if (rc != G3H_OK) return rc;
+  }
+  const fr_t* tw = inverse ? c->d_tw_inv : c->d_tw_fwd;
+  const fr_t* scale_load = (!inverse && coset) ? c->d_coset_fwd : nullptr;
+  const fr_t* scale_store = (inverse && coset) ? c->d_coset_inv : nullptr;
+  const bool store_const = inverse && !coset;
+  if (k <= kSmallMaxLog) {
+    return run(c, "small_ntt", [&] {
+      k_small_ntt<<<1, 32, 0, c->stream>>>(data, tw, scale_load, scale_store, c->h_consts[4],
+                                            store_const ? 1u : 0u, k, check, c->d_err);
+    });
+  }
+  const Plan pl = plan_for(k);
+  fr_t* s = c->d_abc;
+  SliceArgs x = base_args(c, flags);
+  x.src[0] = data;
+  x.dst[0] = s;
+  x.tw = tw;
+  x.scale_tab = scale_load;
+  x.kk = pl.kk[0];
+  x.mode = (check ? SL_CHECK : 0u) | (scale_load ? SL_SCALE_TABLE : 0u);
+  int rc = launch_slice(c, "ntt_brev", k_ntt_brev, x, 1);
+  for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
+    SliceArgs y = base_args(c, flags);
+    const bool top = lvl == pl.levels - 1;
+    y.src[0] = s;
+    y.dst[0] = top ? data : s;
+    y.tw = tw;
+    y.kk = pl.kk[lvl];
+    y.c0 = pl.c0[lvl];
+    if (top) {
+      if (scale_store) {
+        y.scale_tab = scale_store;
+        y.mode = SL_SCALE_TABLE;
+      } else if (store_const) {
+        y.kscale = c->h_consts[4];
+        y.mode = SL_SCALE_CONST;
+      }
+    }
+    rc = launch_slice(c, "ntt_dit", k_ntt_dit, y, 1);
+  }
+  return rc;
+}
+
+bool validate_csr(const g3h_csr* m, size_t n, uint32_t n_wires, int* rc) {
+  if (m->n_rows > n) {
+    *rc = G3H_E_INVAL;
+    return false;
+  }
+  if (!m->row_ptr) {
+    *rc = G3H_E_INVAL;
+    return false;
+  }
+  if (m->row_ptr[0] != 0) {
+    *rc = G3H_E_RANGE;
+    return false;
+  }
+  for (uint32_t i = 0; i < m->n_rows; i++) {
+    if (m->row_ptr[i + 1] < m->row_ptr[i]) {
+      *rc = G3H_E_RANGE;
+      return false;
+    }
+  }
+  const size_t nnz = m->row_ptr[m->n_rows];
+  if (nnz && (!m->col || !m->val)) {
+    *rc = G3H_E_INVAL;
+    return false;
+  }
+  for (size_t k = 0; k < nnz; k++) {
+    if (m->col[k] >= n_wires) {
+      *rc = G3H_E_RANGE;
+      return false;
+    }
+    if (!host_canonical(m->val + 8 * k)) {
+      *rc = G3H_E_NONCANON;
+      return false;
+    }
+  }
+  return true;
+}
+
+int upload_csr(g3h_ctx* c, const g3h_csr* m, uint32_t** rp, uint32_t** col, fr_t** val) {
+  const size_t nnz = m->row_ptr[m->n_rows];
+  int rc = dalloc(rp, (size_t)m->n_rows + 1);
+  if (rc == G3H_OK) rc = dalloc(col, nnz);
+  if (rc == G3H_OK) rc = dalloc(val, nnz);
+  if (rc != G3H_OK) return rc;
+  rc = h2d(c, *rp, m->row_ptr, ((size_t)m->n_rows + 1) * sizeof(uint32_t));
+  if (rc == G3H_OK) rc = h2d(c, *col, m->col, nnz * sizeof(uint32_t));
+  if (rc == G3H_OK) rc = h2d(c, *val, m->val, nnz * sizeof(fr_t));
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_csr* B,
+                int device, void* stream, g3h_ctx** out) {
+  if (!out) return G3H_E_INVAL;
+  *out = nullptr;
+  if (log_n > G3H_MAX_LOG_N) return G3H_E_RANGE;
+  if ((A == nullptr) != (B == nullptr)) return G3H_E_INVAL;
+  const size_t n = (size_t)1 << log_n;
+  int rc = G3H_OK;
+  if (A && (!validate_csr(A, n, n_wires, &rc) || !validate_csr(B, n, n_wires, &rc))) return rc;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+    return G3H_E_CUDA;
+  DeviceGuard guard(device);
+  g3h_ctx* c = new (std::nothrow) g3h_ctx();
+  if (!c) return G3H_E_NOMEM;
+  c->device = device;
+  c->log_n = log_n;
+  c->n = n;
+  c->n_wires = n_wires;
+  if (stream) {
+    c->stream = (cudaStream_t)stream;
+  } else {
+    if (cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking) != cudaSuccess) {
+      delete c;
+      return G3H_E_CUDA;
+    }
+    c->own_stream = true;
+  }
+  rc = set_smem_limits();
+  if (rc == G3H_OK) rc = dalloc(&c->d_err, 1);
+  if (rc == G3H_OK)
+    rc = cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->stream) == cudaSuccess ? G3H_OK
+                                                                                  : G3H_E_CUDA;
+  if (rc == G3H_OK) rc = dalloc(&c->d_consts, 6);
+  if (rc == G3H_OK) rc = dalloc(&c->d_tw_fwd, n / 2);
+  if (rc == G3H_OK) rc = dalloc(&c->d_tw_inv, n / 2);
+  if (rc == G3H_OK) rc = dalloc(&c->d_shift_br, n);
+  if (rc == G3H_OK) rc = dalloc(&c->d_abc, 3 * n);
+  if (rc == G3H_OK)
+    rc = run(c, "tables", [&] { k_domain<<<1, 1, 0, c->stream>>>(c->d_consts, log_n); });
+  if (rc == G3H_OK) rc = build_table(c, c->d_tw_fwd, n / 2, 0, -1, 0);
+  if (rc == G3H_OK) rc = build_table(c, c->d_tw_inv, n / 2, 1, -1, 0);
+  if (rc == G3H_OK) rc = build_table(c, c->d_shift_br, n, 2, 4, log_n);
+  if (rc == G3H_OK && A) {
+    c->has_csr = true;
+    c->n_rows_a = A->n_rows;
+    c->n_rows_b = B->n_rows;
+    rc = upload_csr(c, A, &c->d_rpa, &c->d_cola, &c->d_vala);
+    if (rc == G3H_OK) rc = upload_csr(c, B, &c->d_rpb, &c->d_colb, &c->d_valb);
+  }
+  if (rc == G3H_OK)
+    rc = cudaMemcpyAsync(c->h_consts, c->d_consts, sizeof(c->h_consts), cudaMemcpyDeviceToHost,
+                         c->stream) == cudaSuccess
+             ? G3H_OK
+             : G3H_E_CUDA;
+  if (rc == G3H_OK) rc = cudaStreamSynchronize(c->stream) == cudaSuccess ? G3H_OK : G3H_E_CUDA;
+  if (rc != G3H_OK) {
+    cudaGetLastError();
+    release(c);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return G3H_OK;
+}
+
+int g3h_compute_h(g3h_ctx* c, const uint32_t* witness, uint32_t* h_mont, uint32_t* h_std,
+                  uint32_t flags) {
+  if (!c || !c->has_csr || !h_mont || !h_std || (!witness && c->n_wires)) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const size_t n = c->n;
+  fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
+  if (flags & G3H_DEVICE_PTRS) {
+    int rc = gather(c, (const fr_t*)witness, s[0], s[1], s[2], flags);
+    if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], (fr_t*)h_mont, (fr_t*)h_std, flags);
+    return rc;
+  }
+  int rc = ensure_stage(c, (size_t)c->n_wires + 2 * n);
+  if (rc != G3H_OK) return rc;
+  fr_t* w = c->d_stage;
+  fr_t* hm = c->d_stage + c->n_wires;
+  fr_t* hs = hm + n;
+  rc = h2d(c, w, witness, (size_t)c->n_wires * sizeof(fr_t));
+  if (rc == G3H_OK) rc = gather(c, w, s[0], s[1], s[2], flags);
+  if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], hm, hs, flags);
+  if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const uint32_t* cc,
+                      uint32_t* h_mont, uint32_t* h_std, uint32_t flags) {
+  if (!c || !a || !b || !cc || !h_mont || !h_std) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const size_t n = c->n;
+  if (flags & G3H_DEVICE_PTRS)
+    return quotient(c, (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, (fr_t*)h_mont,
+                    (fr_t*)h_std, flags);
+  int rc = ensure_stage(c, 5 * n);
+  if (rc != G3H_OK) return rc;
+  fr_t* in = c->d_stage;
+  fr_t* hm = c->d_stage + 3 * n;
+  fr_t* hs = hm + n;
+  rc = h2d(c, in, a, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = h2d(c, in + n, b, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = h2d(c, in + 2 * n, cc, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = quotient(c, in, in + n, in + 2 * n, hm, hs, flags);
+  if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_gather(g3h_ctx* c, const uint32_t* witness, uint32_t* a, uint32_t* b, uint32_t* cc,
+               uint32_t flags) {
+  if (!c || !c->has_csr || !a || !b || !cc || (!witness && c->n_wires)) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const size_t n = c->n;
+  if (flags & G3H_DEVICE_PTRS)
+    return gather(c, (const fr_t*)witness, (fr_t*)a, (fr_t*)b, (fr_t*)cc, flags);
+  int rc = ensure_stage(c, (size_t)c->n_wires + 3 * n);
+  if (rc != G3H_OK) return rc;
+  fr_t* w = c->d_stage;
+  fr_t* o = c->d_stage + c->n_wires;
+  rc = h2d(c, w, witness, (size_t)c->n_wires * sizeof(fr_t));
+  if (rc == G3H_OK) rc = gather(c, w, o, o + n, o + 2 * n, flags);
+  if (rc == G3H_OK) rc = d2h(c, a, o, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = d2h(c, b, o + n, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = d2h(c, cc, o + 2 * n, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_ntt(g3h_ctx* c, uint32_t* data, int inverse, int coset, uint32_t flags) {
+  if (!c || !data) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const size_t n = c->n;
+  if (flags & G3H_DEVICE_PTRS) return ntt(c, (fr_t*)data, inverse, coset, flags);
+  int rc = ensure_stage(c, n);
+  if (rc != G3H_OK) return rc;
+  rc = h2d(c, c->d_stage, data, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = ntt(c, c->d_stage, inverse, coset, flags);
+  if (rc == G3H_OK) rc = d2h(c, data, c->d_stage, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_join(g3h_ctx* c, const uint32_t* ea, const uint32_t* eb, const uint32_t* ec,
+             uint32_t* h_mont, uint32_t* h_std, uint32_t flags) {
+  if (!c || !ea || !eb || !ec || !h_mont || !h_std) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const size_t n = c->n;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  auto launch = [&](const fr_t* x, const fr_t* y, const fr_t* z, fr_t* hm, fr_t* hs) {
+    return run(c, "join", [&] {
+      k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(x, y, z, hm, hs, n, check, c->d_err);
+    });
+  };
+  if (flags & G3H_DEVICE_PTRS)
+    return launch((const fr_t*)ea, (const fr_t*)eb, (const fr_t*)ec, (fr_t*)h_mont,
+                  (fr_t*)h_std);
+  int rc = ensure_stage(c, 5 * n);
+  if (rc != G3H_OK) return rc;
+  fr_t* in = c->d_stage;
+  rc = h2d(c, in, ea, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = h2d(c, in + n, eb, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = h2d(c, in + 2 * n, ec, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = launch(in, in + n, in + 2 * n, in + 3 * n, in + 4 * n);
+  if (rc == G3H_OK) rc = d2h(c, h_mont, in + 3 * n, n * sizeof(fr_t));
+  if (rc == G3H_OK) rc = d2h(c, h_std, in + 4 * n, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_mul(g3h_ctx* c, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t count,
+            uint32_t flags) {
+  if (!c || ((!a || !b || !out) && count)) return G3H_E_INVAL;
+  if (count == 0) return G3H_OK;
+  DeviceGuard guard(c->device);
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  auto launch = [&](const fr_t* x, const fr_t* y, fr_t* o) {
+    return run(c, "mul", [&] {
+      k_mul<<<blocks_for(count, 256), 256, 0, c->stream>>>(x, y, o, count, check, c->d_err);
+    });
+  };
+  if (flags & G3H_DEVICE_PTRS) return launch((const fr_t*)a, (const fr_t*)b, (fr_t*)out);
+  int rc = ensure_stage(c, 3 * count);
+  if (rc != G3H_OK) return rc;
+  fr_t* in = c->d_stage;
+  rc = h2d(c, in, a, count * sizeof(fr_t));
+  if (rc == G3H_OK) rc = h2d(c, in + count, b, count * sizeof(fr_t));
+  if (rc == G3H_OK) rc = launch(in, in + count, in + 2 * count);
+  if (rc == G3H_OK) rc = d2h(c, out, in + 2 * count, count * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_sync(g3h_ctx* c) {
+  if (!c) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  return finish(c);
+}
+
+void g3h_destroy(g3h_ctx* c) {
+  if (!c) return;
+  DeviceGuard guard(c->device);
+  cudaStreamSynchronize(c->stream);
+  release(c);
+  delete c;
+}
+
+const char* g3h_strerror(int code) {
+  switch (code) {
+    case G3H_OK: return "ok";
+    case G3H_E_INVAL: return "invalid argument";
+    case G3H_E_NONCANON: return "input field element not canonical (>= r)";
+    case G3H_E_RANGE: return "value out of range (log_n, CSR row pointers or column index)";
+    case G3H_E_NOMEM: return "out of memory";
+    case G3H_E_CUDA: return "CUDA runtime error";
+    default: return "unknown error";
+  }
+}
+
+int g3h_info(const g3h_ctx* c, uint32_t* log_n, uint32_t* n_wires) {
+  if (!c) return G3H_E_INVAL;
+  if (log_n) *log_n = c->log_n;
+  if (n_wires) *n_wires = c->n_wires;
+  return G3H_OK;
+}
+
+int g3h_timing_enable(g3h_ctx* c, int enable) {
+  if (!c) return G3H_E_INVAL;
+  if (enable) {
+    c->launches.clear();
+    c->events_used = 0;
+  }
+  c->timing = enable != 0;
+  return G3H_OK;
+}
+
+int g3h_timing_read(g3h_ctx* c, g3h_kernel_time* out, int max, int* count) {
+  if (!c || (!out && max > 0)) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
+  std::vector<g3h_kernel_time> agg;
+  for (const TimedLaunch& l : c->launches) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, l.e0, l.e1) != cudaSuccess) return G3H_E_CUDA;
+    size_t i = 0;
+    while (i < agg.size() && std::strcmp(agg[i].name, l.name) != 0) i++;
+    if (i == agg.size()) agg.push_back({l.name, 0u, 0.0});
+    agg[i].launches++;
+    agg[i].ms += ms;
+  }
+  for (int i = 0; i < max && i < (int)agg.size(); i++) out[i] = agg[i];
+  if (count) *count = (int)agg.size();
+  return G3H_OK;
+}
+
+}  // extern "C"

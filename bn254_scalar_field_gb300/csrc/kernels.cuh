@@ -1,0 +1,256 @@
+// Gather, join, pointwise product, the small-domain path and the table builders.
+#pragma once
+#include "fr.cuh"
+#include "ntt.cuh"
+
+namespace g3h {
+
+// ---------------------------------------------------------------------------------------
+// Step 1 (GATHER_CU, g16_gather_abc): a_i = sum over CSR row i of A.val[k] * w[A.col[k]],
+// b_i likewise, c_i = a_i * b_i, for i < n; rows at or beyond a matrix's n_rows are empty.
+// One thread per row, as on the page: the rows are short (mean 1-4 terms), ragged and
+// half empty, so a cooperative mapping would idle most lanes. Outputs are canonical.
+// Launch: ceil(n / 256) blocks of 256.
+__global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa,
+                                                const uint32_t* __restrict__ cola,
+                                                const fr_t* __restrict__ vala,
+                                                const uint32_t* __restrict__ rpb,
+                                                const uint32_t* __restrict__ colb,
+                                                const fr_t* __restrict__ valb,
+                                                const fr_t* __restrict__ w, uint32_t n_rows_a,
+                                                uint32_t n_rows_b, uint32_t n, fr_t* a_out,
+                                                fr_t* b_out,
+                                                fr_t* c_out, uint32_t check, uint32_t* err) {
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  fr_t a = fr_zero(), b = fr_zero();
+  if (i < n_rows_a) {
+    for (uint32_t kx = rpa[i], ke = rpa[i + 1]; kx < ke; kx++) {
+      const fr_t wv = fr_ldg(w + cola[kx]);
+      if (check) check_canonical(wv, err);
+      a = fr_add(a, fr_mul(fr_ldg(vala + kx), wv));
+    }
+  }
+  if (i < n_rows_b) {
+    for (uint32_t kx = rpb[i], ke = rpb[i + 1]; kx < ke; kx++) {
+      const fr_t wv = fr_ldg(w + colb[kx]);
+      if (check) check_canonical(wv, err);
+      b = fr_add(b, fr_mul(fr_ldg(valb + kx), wv));
+    }
+  }
+  a = fr_canon(a);
+  b = fr_canon(b);
+  fr_store(a_out + i, a);
+  fr_store(b_out + i, b);
+  fr_store(c_out + i, fr_canon(fr_mul(a, b)));
+}
+
+// Step 5 alone (POINTWISE_CU, g16_h_join): h = a*b - c in both encodings.
+// Launch: ceil(n / 256) blocks of 256.
+__global__ void __launch_bounds__(256) k_join(const fr_t* a, const fr_t* b, const fr_t* c,
+                                              fr_t* h_mont, fr_t* h_std, size_t n,
+                                              uint32_t check, uint32_t* err) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const fr_t x = fr_load(a + i), y = fr_load(b + i), z = fr_load(c + i);
+  if (check) {
+    check_canonical(x, err);
+    check_canonical(y, err);
+    check_canonical(z, err);
+  }
+  const fr_t h = fr_canon(fr_sub(fr_mul(x, y), z));
+  fr_store(h_mont + i, h);
+  fr_store(h_std + i, fr_from_mont(h));
+}
+
+// out = a * b (Montgomery product), canonical. Launch: ceil(n / 256) blocks of 256.
+__global__ void __launch_bounds__(256) k_mul(const fr_t* a, const fr_t* b, fr_t* out, size_t n,
+                                             uint32_t check, uint32_t* err) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const fr_t x = fr_load(a + i), y = fr_load(b + i);
+  if (check) {
+    check_canonical(x, err);
+    check_canonical(y, err);
+  }
+  fr_store(out + i, fr_canon(fr_mul(x, y)));
+}
+
+// ---------------------------------------------------------------------------------------
+// Domains of at most 2^5 points: one block of 32 threads, every pass a loop over
+// butterflies through shared memory (the plain radix-2 schedule; such domains are too
+// small to fill slices of eight elements per thread).
+constexpr uint32_t kSmallMaxLog = 5;
+
+// Steps 2-5 on a, b, c: decimation-in-frequency inverse (tw_inv), shift by
+// shift_br[p] = g^brev(p) / n, decimation-in-time forward (tw_fwd), join.
+// Launch: 1 block of 32 threads.
+__global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t* b,
+                                                       const fr_t* c, const fr_t* tw_inv,
+                                                       const fr_t* tw_fwd,
+                                                       const fr_t* shift_br, fr_t* h_mont,
+                                                       fr_t* h_std, uint32_t k,
+                                                       uint32_t check, uint32_t* err) {
+  __shared__ fr_t s[3][1u << kSmallMaxLog];
+  const uint32_t tid = threadIdx.x, n = 1u << k;
+  const fr_t* in[3] = {a, b, c};
+  for (uint32_t v = 0; v < 3; v++) {
+    for (uint32_t i = tid; i < n; i += blockDim.x) {
+      s[v][i] = fr_load(in[v] + i);
+      if (check) check_canonical(s[v][i], err);
+    }
+  }
+  __syncthreads();
+  for (int bb = (int)k - 1; bb >= 0; bb--) {
+    const uint32_t bit = (uint32_t)bb;
+    for (uint32_t v = 0; v < 3; v++) {
+      for (uint32_t f = tid; f < n / 2; f += blockDim.x) {
+        const uint32_t j = f & ((1u << bit) - 1u);
+        const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
+        const fr_t u = s[v][lo], w = s[v][hi];
+        s[v][lo] = fr_add(u, w);
+        s[v][hi] = fr_mul(fr_sub(u, w), tw_inv[j << (k - 1u - bit)]);
+      }
+    }
+    __syncthreads();
+  }
+  for (uint32_t v = 0; v < 3; v++)
+    for (uint32_t i = tid; i < n; i += blockDim.x) s[v][i] = fr_mul(s[v][i], shift_br[i]);
+  __syncthreads();
+  for (uint32_t bit = 0; bit < k; bit++) {
+    for (uint32_t v = 0; v < 3; v++) {
+      for (uint32_t f = tid; f < n / 2; f += blockDim.x) {
+        const uint32_t j = f & ((1u << bit) - 1u);
+        const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
+        const fr_t u = s[v][lo];
+        const fr_t w = fr_mul(s[v][hi], tw_fwd[j << (k - 1u - bit)]);
+        s[v][lo] = fr_add(u, w);
+        s[v][hi] = fr_sub(u, w);
+      }
+    }
+    __syncthreads();
+  }
+  for (uint32_t i = tid; i < n; i += blockDim.x) {
+    const fr_t h = fr_canon(fr_sub(fr_mul(s[0][i], s[1][i]), s[2][i]));
+    fr_store(h_mont + i, h);
+    fr_store(h_std + i, fr_from_mont(h));
+  }
+}
+
+// A natural-order transform of one small vector in place: position p loads
+// data[brev(p)] (times scale_load[brev(p)] if given), decimation-in-time passes with tw,
+// stores times scale_store[p] if given, else times kscale if given.
+// Launch: 1 block of 32 threads.
+__global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_t* tw,
+                                                  const fr_t* scale_load,
+                                                  const fr_t* scale_store, fr_t kscale,
+                                                  uint32_t use_kscale, uint32_t k,
+                                                  uint32_t check, uint32_t* err) {
+  __shared__ fr_t s[1u << kSmallMaxLog];
+  const uint32_t tid = threadIdx.x, n = 1u << k;
+  for (uint32_t i = tid; i < n; i += blockDim.x) {
+    const uint32_t j = bitrev(i, k);
+    fr_t x = fr_load(data + j);
+    if (check) check_canonical(x, err);
+    if (scale_load) x = fr_mul(x, scale_load[j]);
+    s[i] = x;
+  }
+  __syncthreads();
+  for (uint32_t bit = 0; bit < k; bit++) {
+    for (uint32_t f = tid; f < n / 2; f += blockDim.x) {
+      const uint32_t j = f & ((1u << bit) - 1u);
+      const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
+      const fr_t u = s[lo];
+      const fr_t w = fr_mul(s[hi], tw[j << (k - 1u - bit)]);
+      s[lo] = fr_add(u, w);
+      s[hi] = fr_sub(u, w);
+    }
+    __syncthreads();
+  }
+  for (uint32_t i = tid; i < n; i += blockDim.x) {
+    fr_t x = s[i];
+    if (scale_store) x = fr_mul(x, scale_store[i]);
+    else if (use_kscale) x = fr_mul(x, kscale);
+    fr_store(data + i, fr_canon(x));
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Tables, built on the device at prepare time and kept resident.
+
+// 2^512 mod r (to enter Montgomery form: x * R^2 * R^-1 = x * R).
+__constant__ uint32_t kR2[8] = {0xae216da7u, 0x1bb8e645u, 0xe35c59e3u, 0x53fe3ab1u,
+                                0x53bb8085u, 0x8c49833du, 0x7f4e44a5u, 0x0216d0b1u};
+// r - 2 (Fermat inversion exponent) and (r - 1) / 2^28.
+__constant__ uint32_t kRm2[8] = {0xefffffffu, 0x43e1f593u, 0x79b97091u, 0x2833e848u,
+                                 0x8181585du, 0xb85045b6u, 0xe131a029u, 0x30644e72u};
+__constant__ uint32_t kOddPart[8] = {0x3e1f593fu, 0x9b970914u, 0x833e8487u, 0x181585d2u,
+                                     0x85045b68u, 0x131a029bu, 0x0644e72eu, 0x00000003u};
+
+__device__ __forceinline__ fr_t fr_one_mont() {
+  fr_t x = fr_zero();
+  x.v[0] = 1u;
+  fr_t r2;
+#pragma unroll
+  for (int i = 0; i < 8; i++) r2.v[i] = kR2[i];
+  return fr_canon(fr_mul(x, r2));
+}
+
+__device__ __forceinline__ fr_t fr_small_mont(uint32_t v) {
+  fr_t x = fr_zero();
+  x.v[0] = v;
+  fr_t r2;
+#pragma unroll
+  for (int i = 0; i < 8; i++) r2.v[i] = kR2[i];
+  return fr_canon(fr_mul(x, r2));
+}
+
+// base^e for a 256-bit exponent given as 8 limbs; Montgomery in and out, canonical.
+__device__ fr_t fr_pow_limbs(const fr_t& base, const uint32_t* e) {
+  fr_t acc = fr_one_mont();
+  for (int i = 255; i >= 0; i--) {
+    acc = fr_mul(acc, acc);
+    if ((e[i >> 5] >> (i & 31)) & 1u) acc = fr_mul(acc, base);
+  }
+  return fr_canon(acc);
+}
+
+__device__ fr_t fr_pow_u32(const fr_t& base, uint32_t e) {
+  fr_t acc = fr_one_mont();
+  for (int i = 31; i >= 0; i--) {
+    acc = fr_mul(acc, acc);
+    if ((e >> i) & 1u) acc = fr_mul(acc, base);
+  }
+  return fr_canon(acc);
+}
+
+// Domain constants for 2^k, Montgomery form: out[0] = omega, out[1] = omega^-1, out[2] = g,
+// out[3] = g^-1, out[4] = n^-1, out[5] = 1. The 2^28-th root of unity is 5^((r-1)/2^28)
+// (5 is a quadratic non-residue mod r); g = that root to the 2^(27-k), omega = g^2.
+// Launch: 1 block of 1 thread.
+__global__ void k_domain(fr_t* out, uint32_t k) {
+  fr_t w = fr_pow_limbs(fr_small_mont(5u), kOddPart);
+  for (uint32_t i = 0; i < 27u - k; i++) w = fr_canon(fr_mul(w, w));
+  const fr_t g = w;
+  const fr_t omega = fr_canon(fr_mul(g, g));
+  out[0] = omega;
+  out[1] = fr_pow_limbs(omega, kRm2);
+  out[2] = g;
+  out[3] = fr_pow_limbs(g, kRm2);
+  out[4] = fr_pow_limbs(fr_small_mont(1u << k), kRm2);
+  out[5] = fr_one_mont();
+}
+
+// tab[i] = scale * base^(bit-reversed i if brev_bits else i), i < count; base and scale
+// are indices into the domain constants (scale < 0: none). Launch: ceil(count/256) x 256.
+__global__ void k_pow_table(fr_t* tab, size_t count, const fr_t* consts, int base_idx,
+                            int scale_idx, uint32_t brev_bits) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const uint32_t e = brev_bits ? bitrev((uint32_t)i, brev_bits) : (uint32_t)i;
+  fr_t x = fr_pow_u32(consts[base_idx], e);
+  if (scale_idx >= 0) x = fr_canon(fr_mul(x, consts[scale_idx]));
+  tab[i] = x;
+}
+
+}  // namespace g3h

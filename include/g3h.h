@@ -1,0 +1,163 @@
+/*
+ * g3h: the Groth16 quotient-evaluation (H) path over the BN254 scalar field Fr, on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("snarkrs_gpu_kernels" pages: GATHER_CU, NTT_CU, POINTWISE_CU), for a
+ * domain of n = 2^log_n points with generator omega and a primitive 2n-th root g, g^2 =
+ * omega:
+ *   1. gather   a_i = sum_j A[i,j] w_j,  b_i = sum_j B[i,j] w_j,  c_i = a_i * b_i
+ *               (GATHER_CU, g16_gather_abc, and "why C is computed here")
+ *   2. iNTT     x = n^-1 * DFT_{omega^-1}(v) for v in {a, b, c}   (NTT_CU header)
+ *   3. shift    x_j <- x_j * g^j                                     (NTT_CU header)
+ *   4. NTT      e = DFT_omega(x): the values on the odd coset g*<omega>
+ *   5. join     h_i = e_a[i] * e_b[i] - e_c[i], no division by Z (POINTWISE_CU, "no
+ *               division by Z(coset)"), written as h_mont (Montgomery) and h_std (the
+ *               integer in [0, r)) in one pass (POINTWISE_CU, "two output buffers").
+ * The 2^28-th root of unity is 5^((r-1)/2^28); omega = w^(2^(28-log_n)) and
+ * g = w^(2^(27-log_n)).
+ *
+ * Layout. A field element is 32 bytes: eight little-endian uint32 limbs, least
+ * significant limb first, no padding. "Montgomery" means the limbs hold x * 2^256 mod r
+ * (arkworks' internal form, POINTWISE_CU "two output buffers"). Every input element must
+ * be canonical (< r); every output element is canonical. Vectors are contiguous arrays of
+ * elements in natural index order.
+ *
+ * Pointers. By default every data pointer passed to a call is a HOST pointer: the call
+ * copies inputs to the device, runs, copies outputs back and returns when they are in
+ * place (pinned host memory makes the copies faster; pageable memory works). With
+ * G3H_DEVICE_PTRS in `flags`, every data pointer of that call is a DEVICE pointer on the
+ * context's device: the call only enqueues work on the context's stream and returns;
+ * g3h_sync waits for it and reports errors found on the device. The caller owns every
+ * buffer it passes; the context owns its tables, its copy of the CSR matrices and its
+ * scratch vectors.
+ *
+ * Errors. Every int-returning call returns G3H_OK (0) or a negative G3H_E_* code; no call
+ * aborts or throws. A failed call leaves the context usable. Input elements that are not
+ * canonical are reported as G3H_E_NONCANON: by the call itself for host pointers, by the
+ * next g3h_sync for device pointers (outputs of that call are then unspecified).
+ *
+ * Threads. A context may be used by one host thread at a time; calls on one context run
+ * in order on its stream. Separate contexts are independent.
+ */
+#ifndef G3H_H
+#define G3H_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define G3H_OK 0
+#define G3H_E_INVAL (-1)    /* NULL pointer, bad size, call not valid for this context */
+#define G3H_E_NONCANON (-2) /* an input field element is >= r */
+#define G3H_E_RANGE (-3)    /* log_n outside [0, 27]; CSR row pointers not monotone, not
+                               starting at 0, or a column index >= n_wires */
+#define G3H_E_NOMEM (-4)    /* device or pinned host allocation failed */
+#define G3H_E_CUDA (-5)     /* a CUDA runtime call failed (no device, launch error, ...) */
+
+/* flags */
+#define G3H_DEVICE_PTRS 0x1u  /* data pointers of this call are device pointers */
+#define G3H_NOCHECK 0x2u      /* skip the canonical-input checks */
+#define G3H_UNFUSED_JOIN 0x4u /* compute_h / compute_h_abc: finish the three forward
+                                 transforms, then run the standalone join kernel, instead
+                                 of the join fused into the last transform's store
+                                 (POINTWISE_CU: the unfused kernel the fused path is
+                                 checked against) */
+
+#define G3H_MAX_LOG_N 27
+
+typedef struct g3h_ctx g3h_ctx;
+
+/* One R1CS coefficient matrix in CSR form (GATHER_CU, "why one thread per row": the CSR
+ * sort). Row i holds the terms row_ptr[i] .. row_ptr[i+1]-1; term k has column col[k]
+ * (a wire index < n_wires) and coefficient val[8k .. 8k+7] (Montgomery). Rows at or
+ * beyond n_rows are empty. All three arrays are host memory, read only during
+ * g3h_prepare. */
+typedef struct {
+  uint32_t n_rows;          /* <= 2^log_n */
+  const uint32_t* row_ptr;  /* n_rows + 1 entries, row_ptr[0] = 0, non-decreasing */
+  const uint32_t* col;      /* row_ptr[n_rows] entries */
+  const uint32_t* val;      /* 8 * row_ptr[n_rows] limbs */
+} g3h_csr;
+
+/* Builds a context for the domain 2^log_n on CUDA device `device` (NTT_CU header: the
+ * host builds the twiddle and shift tables once at prepare time and leaves them
+ * resident). A and B are copied to the device. A and B may both be NULL: the context
+ * then serves g3h_compute_h_abc, g3h_ntt, g3h_join and g3h_mul only. `stream` is a
+ * cudaStream_t to run on (cudaStreamLegacy for the legacy default stream), or NULL for a
+ * non-blocking stream the context creates and owns.
+ * On success *out receives the context; on failure *out is NULL.
+ * Errors: G3H_E_INVAL (out NULL, only one of A/B given, n_rows > 2^log_n, NULL array
+ * with a non-zero size), G3H_E_RANGE, G3H_E_NONCANON (a coefficient >= r), G3H_E_NOMEM,
+ * G3H_E_CUDA. */
+int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_csr* B,
+                int device, void* stream, g3h_ctx** out);
+
+/* The whole path, steps 1-5: witness (n_wires elements, Montgomery) -> h_mont, h_std
+ * (n elements each). Needs a context prepared with A and B. */
+int g3h_compute_h(g3h_ctx* ctx, const uint32_t* witness, uint32_t* h_mont, uint32_t* h_std,
+                  uint32_t flags);
+
+/* Steps 2-5 on given evaluation vectors a, b, c (n elements each, Montgomery): the
+ * pages' stages after the gather, for callers that already hold a, b and c. */
+int g3h_compute_h_abc(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, const uint32_t* c,
+                      uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
+
+/* Step 1 alone: a, b, c (n elements each, Montgomery) from the witness. */
+int g3h_gather(g3h_ctx* ctx, const uint32_t* witness, uint32_t* a, uint32_t* b, uint32_t* c,
+               uint32_t flags);
+
+/* One transform of n elements in place (NTT_CU: the transform pair of the path):
+ *   inverse = 0: x <- DFT_omega(y) where y = x, or y_j = x_j * g^j when coset != 0
+ *   inverse = 1: x <- n^-1 DFT_omega^-1(x), then x_j <- x_j * g^-j when coset != 0
+ * so an inverse call undoes the forward call with the same coset setting. */
+int g3h_ntt(g3h_ctx* ctx, uint32_t* data, int inverse, int coset, uint32_t flags);
+
+/* Step 5 alone (POINTWISE_CU g16_h_join): h = ea * eb - ec elementwise over n elements,
+ * written in both encodings. */
+int g3h_join(g3h_ctx* ctx, const uint32_t* ea, const uint32_t* eb, const uint32_t* ec,
+             uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
+
+/* out_i = a_i * b_i (Montgomery product, canonical) for i < count: the product the gather
+ * forms for C (GATHER_CU, "why C is computed here"), e.g. to build c = a * b for
+ * g3h_compute_h_abc. */
+int g3h_mul(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t count,
+            uint32_t flags);
+
+/* Waits for all work enqueued on the context's stream; returns G3H_E_NONCANON if a
+ * device-side input check failed since the last sync (and clears it), G3H_E_CUDA on a
+ * CUDA error. */
+int g3h_sync(g3h_ctx* ctx);
+
+/* Frees the context and everything it owns (waits for its stream first). NULL is a
+ * no-op. */
+void g3h_destroy(g3h_ctx* ctx);
+
+/* A static string describing an error code. */
+const char* g3h_strerror(int code);
+
+/* Domain of a context: log_n and n_wires, or G3H_E_INVAL for NULL. */
+int g3h_info(const g3h_ctx* ctx, uint32_t* log_n, uint32_t* n_wires);
+
+/* Per-kernel device timing, for measurement: with `enable` != 0 the context records a CUDA
+ * event pair on its stream around every kernel it launches, until disabled. Enabling
+ * clears the previous records. */
+int g3h_timing_enable(g3h_ctx* ctx, int enable);
+
+/* Aggregates the recorded launches per kernel name after waiting for the stream: up to
+ * `max` entries (name, number of launches, summed device milliseconds); *count receives
+ * the number of distinct kernels. Names are static strings. */
+typedef struct {
+  const char* name;
+  uint32_t launches;
+  double ms;
+} g3h_kernel_time;
+int g3h_timing_read(g3h_ctx* ctx, g3h_kernel_time* out, int max, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* G3H_H */

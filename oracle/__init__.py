@@ -46,6 +46,7 @@ def lib():
         L.orc_fr_mul.argtypes = [P, P, P]
         L.orc_fr_add.argtypes = [P, P, P]
         L.orc_fr_sub.argtypes = [P, P, P]
+        L.orc_fr_mul_vec.argtypes = [P, P, P, S]
         L.orc_from_mont.argtypes = [P, P, S]
         L.orc_to_mont.argtypes = [P, P, S]
         L.orc_domain.argtypes = [U, P, P]
@@ -103,6 +104,15 @@ def fr_sub(a, b):
     out = np.empty_like(a)
     for i in range(a.shape[0]):
         lib().orc_fr_sub(_p(a[i]), _p(b[i]), _p(out[i]))
+    return out
+
+
+def fr_mul_vec(a, b):
+    """Elementwise Montgomery product of two (m, 8) arrays."""
+    a, b = _fr(a), _fr(b)
+    assert a.shape == b.shape
+    out = np.empty_like(a)
+    lib().orc_fr_mul_vec(_p(a), _p(b), _p(out), a.shape[0])
     return out
 
 

@@ -1,0 +1,294 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle, bit for bit.
+
+Field arithmetic is exact, so the bar is equality of every limb of every element. Sizes
+run from 2^0 through the four proving-key-shaped domains (2^12, 2^14, 2^17, 2^18) to the
+2^22 stress vectors, covering every slice geometry the launch plan uses: the small
+one-block path (2^0..2^5), two levels with equal and unequal halves (2^6..2^22), and
+three levels (2^23). Ragged cases: constraint rows fewer than the domain, empty
+matrices, a single-row domain.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bn254_scalar_field_gb300 import build, g3h, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    oracle.build()
+    yield
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dev(x):
+    torch = _torch()
+    return torch.from_numpy(x.view(np.int32)).cuda()
+
+
+def _host(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def _zeros(n):
+    return np.zeros((n, 8), np.uint32)
+
+
+def _edge_fr():
+    from oracle import fr_int as F
+
+    r = F.R_MOD
+    vals = [0, 1, 2, r - 1, r - 2, (1 << 256) % r, (1 << 253), (r - 1) // 2, 0xFFFFFFFF,
+            (1 << 32), (1 << 224) - 1, r - (1 << 128)]
+    return F.ints_to_array(vals)
+
+
+# -------------------------------------------------------------------------- field ----
+
+def test_mul_edge_and_random_values():
+    a = np.concatenate([_edge_fr(), synth.uniform_fr(synth.SplitMix64(1), 5000)])
+    b = np.concatenate([_edge_fr()[::-1], synth.uniform_fr(synth.SplitMix64(2), 5000)])
+    # every edge value against every edge value
+    e = _edge_fr()
+    ea = np.repeat(e, e.shape[0], axis=0)
+    eb = np.tile(e, (e.shape[0], 1))
+    a = np.concatenate([a, ea])
+    b = np.concatenate([b, eb])
+    with g3h.Context(4) as ctx:
+        out = _zeros(a.shape[0])
+        ctx.mul(a, b, out)
+    assert np.array_equal(out, oracle.fr_mul_vec(a, b))
+
+
+# ---------------------------------------------------------------------- transforms ----
+
+NTT_SIZES = list(range(0, 13)) + [13, 14, 16, 17, 18]
+
+
+@pytest.mark.parametrize("log_n", NTT_SIZES)
+def test_ntt_all_modes(log_n):
+    n = 1 << log_n
+    x = synth.uniform_fr(synth.SplitMix64(100 + log_n), n)
+    with g3h.Context(log_n) as ctx:
+        for inverse in (False, True):
+            for coset in (False, True):
+                got = x.copy()
+                ctx.ntt(got, inverse=inverse, coset=coset)
+                want = oracle.ntt(x, log_n, inverse=inverse, coset=coset)
+                assert np.array_equal(got, want), (inverse, coset)
+
+
+@pytest.mark.parametrize("log_n", [20, 23])
+def test_ntt_large_and_three_levels(log_n):
+    n = 1 << log_n
+    x = synth.uniform_fr(synth.SplitMix64(200 + log_n), n)
+    with g3h.Context(log_n) as ctx:
+        got = x.copy()
+        ctx.ntt(got, coset=True)
+        assert np.array_equal(got, oracle.ntt(x, log_n, coset=True))
+        ctx.ntt(got, inverse=True, coset=True)
+        assert np.array_equal(got, x)
+
+
+# -------------------------------------------------------------------------- gather ----
+
+@pytest.mark.parametrize("log_n", [0, 1, 3, 7, 10, 12, 14])
+def test_gather(log_n):
+    A, B, w = synth.problem(log_n, seed=300 + log_n)
+    n = 1 << log_n
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        a, b, c = _zeros(n), _zeros(n), _zeros(n)
+        ctx.gather(w, a, b, c)
+    ra, rb, rc = oracle.gather(log_n, A, B, w)
+    assert np.array_equal(a, ra) and np.array_equal(b, rb) and np.array_equal(c, rc)
+
+
+def test_join_unfused_kernel():
+    n = 1 << 11
+    rng = synth.SplitMix64(77)
+    ea, eb, ec = (synth.uniform_fr(rng, n) for _ in range(3))
+    with g3h.Context(11) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.join(ea, eb, ec, hm, hs)
+    prod = oracle.fr_mul_vec(ea, eb)
+    want = np.stack([oracle.fr_sub(prod[i:i + 1], ec[i:i + 1])[0] for i in range(n)])
+    assert np.array_equal(hm, want)
+    assert np.array_equal(hs, oracle.from_mont(want))
+
+
+# --------------------------------------------------------------------- whole path ----
+
+@pytest.mark.parametrize("log_n", list(range(0, 12)))
+def test_compute_h_small_domains(log_n):
+    A, B, w = synth.problem(log_n, seed=400 + log_n)
+    n = 1 << log_n
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm, hs)
+    want_m, want_s = oracle.compute_h(log_n, A, B, w)
+    assert np.array_equal(hm, want_m)
+    assert np.array_equal(hs, want_s)
+
+
+@pytest.mark.parametrize("log_n", [12, 14, 17, 18])
+def test_compute_h_proving_key_configs(log_n):
+    """The four proving-key-shaped workloads, every output element compared."""
+    A, B, w = synth.problem(log_n)
+    n = 1 << log_n
+    want_m, want_s = oracle.compute_h(log_n, A, B, w)
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm, hs)
+        assert np.array_equal(hm, want_m)
+        assert np.array_equal(hs, want_s)
+        # the unfused join path (POINTWISE_CU: the reference the fused path is checked
+        # against) gives the same bits
+        hm2, hs2 = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_UNFUSED_JOIN)
+        assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
+        # device pointers, asynchronous on the context's stream, twice in a row
+        torch = _torch()
+        wd = _dev(w)
+        for _ in range(2):
+            hmd = torch.zeros((n, 8), dtype=torch.int32, device="cuda")
+            hsd = torch.zeros((n, 8), dtype=torch.int32, device="cuda")
+            ctx.compute_h(wd, hmd, hsd)
+            ctx.sync()
+            assert np.array_equal(_host(hmd), want_m)
+            assert np.array_equal(_host(hsd), want_s)
+
+
+def test_compute_h_abc_stress_2_22():
+    """The 2^22 NTT stress workload: a, b uniform, c = a*b, every element compared."""
+    log_n = synth.STRESS_LOG_N
+    n = 1 << log_n
+    a, b = synth.stress_ab(log_n)
+    c = oracle.fr_mul_vec(a, b)
+    want_m, want_s = oracle.compute_h_abc(log_n, a, b, c)
+    with g3h.Context(log_n) as ctx:
+        c_gpu = _zeros(n)
+        ctx.mul(a, b, c_gpu)
+        assert np.array_equal(c_gpu, c)
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h_abc(a, b, c, hm, hs)
+    assert np.array_equal(hm, want_m)
+    assert np.array_equal(hs, want_s)
+
+
+def test_compute_h_abc_three_levels():
+    log_n = 23
+    n = 1 << log_n
+    rng = synth.SplitMix64(523)
+    a, b, c = (synth.uniform_fr(rng, n) for _ in range(3))
+    want_m, want_s = oracle.compute_h_abc(log_n, a, b, c)
+    with g3h.Context(log_n) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h_abc(a, b, c, hm, hs)
+    assert np.array_equal(hm, want_m) and np.array_equal(hs, want_s)
+
+
+# --------------------------------------------------------------------- edge cases ----
+
+def test_ragged_rows_and_empty_matrices():
+    log_n = 9
+    n = 1 << log_n
+    A, B, w = synth.problem(log_n, seed=9)
+    # fewer CSR rows than the domain: truncate both matrices to 300 and 123 rows
+    def cut(m, rows):
+        rp = m[0][:rows + 1].copy()
+        nnz = int(rp[-1])
+        return rp, m[1][:nnz].copy(), m[2][:nnz].copy()
+
+    A2, B2 = cut(A, 300), cut(B, 123)
+    with g3h.Context(log_n, w.shape[0], A2, B2) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm, hs)
+    # the oracle takes one row count: pad the shorter matrices with empty rows
+    def pad(m, rows):
+        rp = np.concatenate([m[0], np.full(rows + 1 - m[0].shape[0], m[0][-1], np.uint32)])
+        return rp, m[1], m[2]
+
+    want_m, want_s = oracle.compute_h(log_n, pad(A2, n), pad(B2, n), w)
+    assert np.array_equal(hm, want_m) and np.array_equal(hs, want_s)
+    # empty matrices: a = b = c = 0, so h = 0
+    E = (np.zeros(n + 1, np.uint32), np.zeros(0, np.uint32), np.zeros((0, 8), np.uint32))
+    with g3h.Context(log_n, w.shape[0], E, E) as ctx:
+        hm, hs = _zeros(n) + 7, _zeros(n) + 7
+        ctx.compute_h(w, hm, hs)
+    assert not hm.any() and not hs.any()
+
+
+def test_noncanonical_inputs_reported_and_context_survives():
+    log_n = 8
+    n = 1 << log_n
+    A, B, w = synth.problem(log_n, seed=5)
+    bad = w.copy()
+    bad[0] = synth.MODULUS_LIMBS  # w[0] is referenced by the gather (the constant wire)
+    bad[1:] = synth.MODULUS_LIMBS
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        with pytest.raises(g3h.G3HError) as ei:
+            ctx.compute_h(bad, hm, hs)
+        assert ei.value.code == g3h.G3H_E_NONCANON
+        # device pointers: reported by the next sync
+        torch = _torch()
+        hmd = torch.zeros((n, 8), dtype=torch.int32, device="cuda")
+        hsd = torch.zeros((n, 8), dtype=torch.int32, device="cuda")
+        ctx.compute_h(_dev(bad), hmd, hsd)
+        with pytest.raises(g3h.G3HError) as ei:
+            ctx.sync()
+        assert ei.value.code == g3h.G3H_E_NONCANON
+        # and the context still computes correctly afterwards
+        ctx.compute_h(w, hm, hs)
+        want_m, want_s = oracle.compute_h(log_n, A, B, w)
+        assert np.array_equal(hm, want_m) and np.array_equal(hs, want_s)
+        x = _zeros(n)
+        x[3] = synth.MODULUS_LIMBS
+        with pytest.raises(g3h.G3HError):
+            ctx.ntt(x)  # in place: x now holds the (unspecified) output
+        x = _zeros(n)
+        x[3] = synth.MODULUS_LIMBS
+        with pytest.raises(g3h.G3HError):
+            ctx.compute_h_abc(x, x, x, hm, hs)
+        with pytest.raises(g3h.G3HError):
+            ctx.join(x, x, x, hm, hs)
+        with pytest.raises(g3h.G3HError):
+            ctx.mul(x, x, hm)
+        # gather: a non-canonical witness value referenced by the matrices
+        a, b, c = _zeros(n), _zeros(n), _zeros(n)
+        with pytest.raises(g3h.G3HError):
+            ctx.gather(bad, a, b, c)
+        # NOCHECK skips the checks: no error raised
+        ctx.mul(x, x, hm, flags=g3h.G3H_NOCHECK)
+
+
+def test_domain_only_context_rejects_compute_h():
+    with g3h.Context(6) as ctx:
+        with pytest.raises(g3h.G3HError) as ei:
+            ctx.compute_h(np.zeros((4, 8), np.uint32), _zeros(64), _zeros(64))
+        assert ei.value.code == g3h.G3H_E_INVAL
+
+
+def test_timing_records_kernels():
+    log_n = 12
+    A, B, w = synth.problem(log_n)
+    n = 1 << log_n
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        ctx.timing_enable(True)
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm, hs)
+        t = ctx.timing_read()
+        ctx.timing_enable(False)
+    assert set(t) == {"gather", "ntt_dif", "ntt_mid", "ntt_dit_join"}
+    assert all(v[0] == 1 and v[1] > 0 for v in t.values())
