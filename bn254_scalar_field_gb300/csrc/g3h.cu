@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -677,3 +678,131 @@ int g3h_timing_read(g3h_ctx* c, g3h_kernel_time* out, int max, int* count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// g3h_compute_h_abc_static: steps 2-5 without any allocation.
+//
+// For callers that cannot allocate device memory themselves or through this library: a
+// framework whose caching allocator must own every device byte, code that runs while its
+// stream is being captured into a CUDA graph (where cudaMalloc is not permitted), or
+// latency-critical paths that cannot afford cudaMalloc's device-wide synchronisation.
+// The working vectors and the domain tables live in one file-scope device array of fixed
+// size, reserved on every GPU that loads this library until the process exits:
+//   [0, 3N)          the three working vectors a, b, c
+//   [3N, 3.5N)       forward twiddles omega^j, j < n/2
+//   [3.5N, 4N)       inverse twiddles omega^-j, j < n/2
+//   [4N, 5N)         shift table g^brev(p) / n
+//   [5N, 5N + 6)     domain constants
+// with N = 2^16, the largest domain this entry point accepts: 5N + 8 elements of 32 bytes,
+// 10 MiB. Every element of the array that a call reads was written earlier in the same
+// call or by the table build for the same domain, so nothing has to start at zero.
+namespace {
+constexpr uint32_t kNoAllocMaxLog = 16;
+constexpr size_t kNoAllocN = (size_t)1 << kNoAllocMaxLog;
+constexpr size_t kNoAllocElems = 5 * kNoAllocN + 8;
+}  // namespace
+
+static __device__ __align__(256) fr_t g3h_noalloc_scratch[kNoAllocElems];
+
+namespace {
+
+struct NoAllocDevice {
+  fr_t* base = nullptr;  // device address of g3h_noalloc_scratch on this device
+  int table_log = -1;    // domain whose tables the array currently holds
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+int noalloc_launch_ok() { return cudaGetLastError() == cudaSuccess ? G3H_OK : G3H_E_CUDA; }
+
+}  // namespace
+
+extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const uint32_t* b,
+                                        const uint32_t* c, uint32_t* h_mont, uint32_t* h_std,
+                                        void* stream) {
+  if (!a || !b || !c || !h_mont || !h_std) return G3H_E_INVAL;
+  if (log_n > kNoAllocMaxLog) return G3H_E_RANGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return G3H_E_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.base) {
+    // One-time set-up on this device (the device is current): the host-side name of the
+    // array is not a device address, so ask the runtime for the address.
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g3h_noalloc_scratch) != cudaSuccess || !p) return G3H_E_CUDA;
+    d.base = (fr_t*)p;
+  }
+  const cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)1 << log_n;
+  fr_t* work = d.base;
+  fr_t* tw_fwd = d.base + 3 * kNoAllocN;
+  fr_t* tw_inv = tw_fwd + kNoAllocN / 2;
+  fr_t* shift = tw_inv + kNoAllocN / 2;
+  fr_t* consts = shift + kNoAllocN;
+  if (d.table_log != (int)log_n) {
+    d.table_log = -1;
+    k_domain<<<1, 1, 0, s>>>(consts, log_n);
+    if (n / 2)
+      k_pow_table<<<blocks_for(n / 2, 256), 256, 0, s>>>(tw_fwd, n / 2, consts, 0, -1, 0);
+    if (n / 2)
+      k_pow_table<<<blocks_for(n / 2, 256), 256, 0, s>>>(tw_inv, n / 2, consts, 1, -1, 0);
+    k_pow_table<<<blocks_for(n, 256), 256, 0, s>>>(shift, n, consts, 2, 4, log_n);
+    if (noalloc_launch_ok() != G3H_OK) return G3H_E_CUDA;
+    d.table_log = (int)log_n;
+  }
+  const fr_t* in[3] = {(const fr_t*)a, (const fr_t*)b, (const fr_t*)c};
+  fr_t* hm = (fr_t*)h_mont;
+  fr_t* hs = (fr_t*)h_std;
+  if (log_n <= kSmallMaxLog) {
+    k_small_quotient<<<1, 32, 0, s>>>(in[0], in[1], in[2], tw_inv, tw_fwd, shift, hm, hs, log_n,
+                                       0u, nullptr);
+    return noalloc_launch_ok();
+  }
+  fr_t* v[3] = {work, work + n, work + 2 * n};
+  const Plan pl = plan_for(log_n);  // two levels: log_n <= 16
+  auto args = [&]() {
+    SliceArgs x;
+    std::memset(&x, 0, sizeof(x));
+    x.log_n = log_n;
+    return x;
+  };
+  auto geometry = [&](const SliceArgs& x, unsigned nvec, dim3* grid, dim3* block, size_t* smem) {
+    *grid = dim3((unsigned)(n >> x.kk), nvec);
+    *block = dim3(1u << (x.kk - 3u));
+    *smem = (size_t)32 << x.kk;
+  };
+  dim3 grid, block;
+  size_t smem;
+  SliceArgs x = args();
+  for (int i = 0; i < 3; i++) {
+    x.src[i] = in[i];
+    x.dst[i] = v[i];
+  }
+  x.tw = tw_inv;
+  x.kk = pl.kk[1];
+  x.c0 = pl.c0[1];
+  geometry(x, 3, &grid, &block, &smem);
+  k_ntt_dif<<<grid, block, smem, s>>>(x);
+  SliceArgs m = args();
+  for (int i = 0; i < 3; i++) m.dst[i] = v[i];
+  m.tw = tw_inv;
+  m.tw2 = tw_fwd;
+  m.scale_tab = shift;
+  m.kk = pl.kk[0];
+  geometry(m, 3, &grid, &block, &smem);
+  k_ntt_mid<<<grid, block, smem, s>>>(m);
+  SliceArgs t = args();
+  for (int i = 0; i < 3; i++) t.src[i] = t.dst[i] = v[i];
+  t.tw = tw_fwd;
+  t.kk = pl.kk[1];
+  t.c0 = pl.c0[1];
+  t.mode = SL_JOIN;
+  t.h_mont = hm;
+  t.h_std = hs;
+  geometry(t, 1, &grid, &block, &smem);
+  k_ntt_dit<<<grid, block, smem, s>>>(t);
+  return noalloc_launch_ok();
+}

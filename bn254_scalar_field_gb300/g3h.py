@@ -32,7 +32,7 @@ CUDA_STREAM_LEGACY = 0x1
 
 ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather", "g3h_ntt",
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
-                "g3h_timing_enable", "g3h_timing_read")
+                "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static")
 
 
 class G3HError(RuntimeError):
@@ -80,6 +80,7 @@ def lib():
         L.g3h_timing_enable.argtypes = [P, I]
         L.g3h_timing_read.argtypes = [P, ctypes.POINTER(g3h_kernel_time), I,
                                       ctypes.POINTER(I)]
+        L.g3h_compute_h_abc_static.argtypes = [U, P, P, P, P, P, P]
         for name in ENTRY_POINTS:
             if name not in ("g3h_destroy", "g3h_strerror"):
                 getattr(L, name).restype = ctypes.c_int
@@ -233,6 +234,21 @@ def g3h_timing_read(ctx):
     _check(lib().g3h_timing_read(ctx, buf, 64, ctypes.byref(count)), "g3h_timing_read")
     return {buf[i].name.decode(): (buf[i].launches, buf[i].ms)
             for i in range(min(count.value, 64))}
+
+
+def g3h_compute_h_abc_static(log_n, a, b, c, h_mont, h_std, stream=None):
+    """Steps 2-5 with no allocation (library-internal fixed array, log_n <= 16). Device
+    tensors on the current device only; `stream` defaults to torch's current stream."""
+    bufs = [_ptr(x, None) for x in (a, b, c, h_mont, h_std)]
+    if any(d is not True for _, d in bufs):
+        raise ValueError("g3h_compute_h_abc_static takes device tensors only")
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(lib().g3h_compute_h_abc_static(log_n, *[p for p, _ in bufs],
+                                          ctypes.c_void_p(stream) if stream else None),
+           "g3h_compute_h_abc_static")
 
 
 class Context:

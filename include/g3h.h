@@ -126,6 +126,33 @@ int g3h_join(g3h_ctx* ctx, const uint32_t* ea, const uint32_t* eb, const uint32_
 int g3h_mul(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t count,
             uint32_t flags);
 
+/* Steps 2-5 like g3h_compute_h_abc, for callers that cannot allocate device memory: a
+ * framework whose caching allocator must own every device byte, code running while its
+ * stream is being captured into a CUDA graph (cudaMalloc is not permitted there), or a
+ * latency-critical path that cannot take cudaMalloc's device-wide synchronisation. It has
+ * no counterpart on the pages; it is this library's own addition.
+ *
+ * It needs no context and allocates nothing: its working vectors and domain tables live in
+ * one fixed device array of 10 MiB inside the library, reserved on every GPU that loads
+ * the library until the process exits. Hence log_n <= 16 (domains up to 2^16 points);
+ * larger domains return G3H_E_RANGE without doing anything.
+ *
+ * a, b, c (inputs, n elements each, Montgomery, canonical; NOT checked) and h_mont, h_std
+ * (outputs, n elements each) are device pointers on the current CUDA device; `stream` is
+ * the cudaStream_t to run on (NULL: the legacy default stream). The call enqueues the work
+ * and returns; the outputs are ready when the stream reaches that point.
+ *
+ * The first call on a device looks up the array's device address (a one-time set-up with
+ * that device current); make that first call before any stream capture begins. A call for
+ * a different log_n than the previous call on that device also rebuilds the tables in the
+ * array (kernel launches only). All calls on a device share the array, so calls that
+ * overlap on the GPU (on different streams, or from different threads without ordering)
+ * race and give wrong results: order them on one stream.
+ * Returns G3H_OK, G3H_E_INVAL (a NULL pointer), G3H_E_RANGE (log_n > 16) or G3H_E_CUDA. */
+int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const uint32_t* b,
+                             const uint32_t* c, uint32_t* h_mont, uint32_t* h_std,
+                             void* stream);
+
 /* Waits for all work enqueued on the context's stream; returns G3H_E_NONCANON if a
  * device-side input check failed since the last sync (and clears it), G3H_E_CUDA on a
  * CUDA error. */
