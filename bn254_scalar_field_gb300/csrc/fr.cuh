@@ -53,44 +53,71 @@ __device__ __forceinline__ fr_t fr_zero() {
   return z;
 }
 
-// a * b * 2^-256 mod r, inputs in [0, 2r), output in [0, 2r).
-//
-// CIOS: for each word b_i of b, t <- (t + a * b_i + m * r) / 2^32 with
-// m = (t + a*b_i) * (-r^{-1}) mod 2^32. Each step of the inner loops is a 32x32 -> 64
-// multiply plus two 32-bit addends, (2^32-1)^2 + 2(2^32-1) = 2^64 - 1, so it never
-// overflows 64 bits; written with 64-bit products the compiler issues wide multiply-adds
-// (measured faster on this GPU than separate low/high multiply chains). On entry to a
-// row t < 3r < 2^256, so t fits eight words plus the carry word t8 of the row.
+// One CIOS row on words t0..t7 (t < 3r < 2^256 on entry): t <- (t + a*bi + m*r) / 2^32,
+// m = (t + a*bi) * (-r^{-1}) mod 2^32. The products of a*bi are added as two carry
+// chains, one over the even limbs a0, a2, a4, a6 (whose low and high words land on word
+// pairs (0,1), (2,3), (4,5), (6,7)) and one over the odd limbs (pairs (1,2) ... (7,8)),
+// so that the low and high word of each product are adjacent in one chain; m*r likewise,
+// and its odd chain writes each word one position down, which is the division by 2^32.
+// The sum before the division is below 3r + 2*2^32*2r < 2^288, so nothing carries out of
+// the ninth word t8.
+#define G3H_CIOS_ROW(t0, t1, t2, t3, t4, t5, t6, t7, bi)                                   \
+  asm("{\n\t"                                                                             \
+      ".reg .u32 m, t8;\n\t"                                                              \
+      "mad.lo.cc.u32  %0, %8,  %16, %0;\n\t"                                              \
+      "madc.hi.cc.u32 %1, %8,  %16, %1;\n\t"                                              \
+      "madc.lo.cc.u32 %2, %10, %16, %2;\n\t"                                              \
+      "madc.hi.cc.u32 %3, %10, %16, %3;\n\t"                                              \
+      "madc.lo.cc.u32 %4, %12, %16, %4;\n\t"                                              \
+      "madc.hi.cc.u32 %5, %12, %16, %5;\n\t"                                              \
+      "madc.lo.cc.u32 %6, %14, %16, %6;\n\t"                                              \
+      "madc.hi.cc.u32 %7, %14, %16, %7;\n\t"                                              \
+      "addc.u32       t8, 0, 0;\n\t"                                                      \
+      "mad.lo.cc.u32  %1, %9,  %16, %1;\n\t"                                              \
+      "madc.hi.cc.u32 %2, %9,  %16, %2;\n\t"                                              \
+      "madc.lo.cc.u32 %3, %11, %16, %3;\n\t"                                              \
+      "madc.hi.cc.u32 %4, %11, %16, %4;\n\t"                                              \
+      "madc.lo.cc.u32 %5, %13, %16, %5;\n\t"                                              \
+      "madc.hi.cc.u32 %6, %13, %16, %6;\n\t"                                              \
+      "madc.lo.cc.u32 %7, %15, %16, %7;\n\t"                                              \
+      "madc.hi.u32    t8, %15, %16, t8;\n\t"                                              \
+      "mul.lo.u32     m,  %0, 0xefffffff;\n\t"                                            \
+      "mad.lo.cc.u32  %0, m, 0xf0000001, %0;\n\t"                                         \
+      "madc.hi.cc.u32 %1, m, 0xf0000001, %1;\n\t"                                         \
+      "madc.lo.cc.u32 %2, m, 0x79b97091, %2;\n\t"                                         \
+      "madc.hi.cc.u32 %3, m, 0x79b97091, %3;\n\t"                                         \
+      "madc.lo.cc.u32 %4, m, 0x8181585d, %4;\n\t"                                         \
+      "madc.hi.cc.u32 %5, m, 0x8181585d, %5;\n\t"                                         \
+      "madc.lo.cc.u32 %6, m, 0xe131a029, %6;\n\t"                                         \
+      "madc.hi.cc.u32 %7, m, 0xe131a029, %7;\n\t"                                         \
+      "addc.u32       t8, t8, 0;\n\t"                                                     \
+      "mad.lo.cc.u32  %0, m, 0x43e1f593, %1;\n\t"                                         \
+      "madc.hi.cc.u32 %1, m, 0x43e1f593, %2;\n\t"                                         \
+      "madc.lo.cc.u32 %2, m, 0x2833e848, %3;\n\t"                                         \
+      "madc.hi.cc.u32 %3, m, 0x2833e848, %4;\n\t"                                         \
+      "madc.lo.cc.u32 %4, m, 0xb85045b6, %5;\n\t"                                         \
+      "madc.hi.cc.u32 %5, m, 0xb85045b6, %6;\n\t"                                         \
+      "madc.lo.cc.u32 %6, m, 0x30644e72, %7;\n\t"                                         \
+      "madc.hi.u32    %7, m, 0x30644e72, t8;\n\t"                                         \
+      "}"                                                                                 \
+      : "+r"(t0), "+r"(t1), "+r"(t2), "+r"(t3), "+r"(t4), "+r"(t5), "+r"(t6), "+r"(t7)   \
+      : "r"(a.v[0]), "r"(a.v[1]), "r"(a.v[2]), "r"(a.v[3]), "r"(a.v[4]), "r"(a.v[5]),    \
+        "r"(a.v[6]), "r"(a.v[7]), "r"(bi))
+
+// a * b * 2^-256 mod r, inputs in [0, 2r), output in [0, 2r) (CIOS: one row per word of
+// b; written with even/odd carry chains because this GPU issues a 32x32 -> 64-bit product
+// at a quarter of the 32-bit multiply rate whether as one wide instruction or as a
+// low/high pair, and the chains above let the compiler issue each product once).
 __device__ __forceinline__ fr_t fr_mul(const fr_t& a, const fr_t& b) {
-  const uint32_t R[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
-  uint32_t t[9];
-#pragma unroll
-  for (int j = 0; j < 9; j++) t[j] = 0;
+  uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0, t4 = 0, t5 = 0, t6 = 0, t7 = 0;
 #pragma unroll
   for (int i = 0; i < 8; i++) {
-    uint64_t c = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-      uint64_t s = (uint64_t)a.v[j] * b.v[i] + t[j] + c;
-      t[j] = (uint32_t)s;
-      c = s >> 32;
-    }
-    t[8] = (uint32_t)c;
-    uint32_t m = t[0] * G3H_NPRIME;
-    uint64_t s = (uint64_t)m * R[0] + t[0];
-    c = s >> 32;
-#pragma unroll
-    for (int j = 1; j < 8; j++) {
-      s = (uint64_t)m * R[j] + t[j] + c;
-      t[j - 1] = (uint32_t)s;
-      c = s >> 32;
-    }
-    t[7] = t[8] + (uint32_t)c;
+    G3H_CIOS_ROW(t0, t1, t2, t3, t4, t5, t6, t7, b.v[i]);
   }
-  fr_t r;
-#pragma unroll
-  for (int j = 0; j < 8; j++) r.v[j] = t[j];
-  return r;
+  fr_t c;
+  c.v[0] = t0; c.v[1] = t1; c.v[2] = t2; c.v[3] = t3;
+  c.v[4] = t4; c.v[5] = t5; c.v[6] = t6; c.v[7] = t7;
+  return c;
 }
 
 // a + b, inputs in [0, 2r), output in [0, 2r): the sum is below 4r < 2^256, and 2r is

@@ -11,6 +11,7 @@
 // All launches go to the context's stream in order; nothing synchronises between them.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -155,7 +156,7 @@ unsigned blocks_for(size_t count, unsigned per) { return (unsigned)((count + per
 int launch_slice(g3h_ctx* c, const char* name, void (*kern)(SliceArgs), const SliceArgs& a,
                  unsigned nvec) {
   const dim3 grid((unsigned)(c->n >> a.kk), nvec);
-  const dim3 block(1u << (a.kk - 3u));
+  const dim3 block(std::min(1u << (a.kk - 1u), kSliceThreads));
   const size_t smem = (size_t)32 << a.kk;
   return run(c, name, [&] { kern<<<grid, block, smem, c->stream>>>(a); });
 }
@@ -771,7 +772,7 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
   };
   auto geometry = [&](const SliceArgs& x, unsigned nvec, dim3* grid, dim3* block, size_t* smem) {
     *grid = dim3((unsigned)(n >> x.kk), nvec);
-    *block = dim3(1u << (x.kk - 3u));
+    *block = dim3(std::min(1u << (x.kk - 1u), kSliceThreads));
     *smem = (size_t)32 << x.kk;
   };
   dim3 grid, block;

@@ -10,6 +10,39 @@ namespace g3h {
 // b_i likewise, c_i = a_i * b_i, for i < n; rows at or beyond a matrix's n_rows are empty.
 // One thread per row, as on the page: the rows are short (mean 1-4 terms), ragged and
 // half empty, so a cooperative mapping would idle most lanes. Outputs are canonical.
+//
+// Most witness values of a circuit are 0 or 1 (bits, flags, the constant wire), so a term
+// whose wire value is 0 contributes nothing and one whose value is the Montgomery form of
+// 1 contributes its coefficient unchanged; only the remaining terms take a multiply, and
+// c is only multiplied out when both a and b are non-zero. These are identities of the
+// field, so the outputs are the same canonical values.
+__device__ __forceinline__ bool fr_is_zero(const fr_t& x) {
+  return (x.v[0] | x.v[1] | x.v[2] | x.v[3] | x.v[4] | x.v[5] | x.v[6] | x.v[7]) == 0u;
+}
+
+// 2^256 mod r: the Montgomery form of 1.
+__device__ __forceinline__ bool fr_is_mont_one(const fr_t& x) {
+  return ((x.v[0] ^ 0x4ffffffbu) | (x.v[1] ^ 0xac96341cu) | (x.v[2] ^ 0x9f60cd29u) |
+          (x.v[3] ^ 0x36fc7695u) | (x.v[4] ^ 0x7879462eu) | (x.v[5] ^ 0x666ea36fu) |
+          (x.v[6] ^ 0x9a07df2fu) | (x.v[7] ^ 0x0e0a77c1u)) == 0u;
+}
+
+__device__ __forceinline__ fr_t gather_row(const uint32_t* __restrict__ rp,
+                                           const uint32_t* __restrict__ col,
+                                           const fr_t* __restrict__ val,
+                                           const fr_t* __restrict__ w, uint32_t i,
+                                           uint32_t check, uint32_t* err) {
+  fr_t acc = fr_zero();
+  for (uint32_t kx = rp[i], ke = rp[i + 1]; kx < ke; kx++) {
+    const fr_t wv = fr_ldg(w + col[kx]);
+    if (check) check_canonical(wv, err);
+    if (fr_is_zero(wv)) continue;
+    const fr_t cv = fr_ldg(val + kx);
+    acc = fr_add(acc, fr_is_mont_one(wv) ? cv : fr_mul(cv, wv));
+  }
+  return fr_canon(acc);
+}
+
 // Launch: ceil(n / 256) blocks of 256.
 __global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa,
                                                 const uint32_t* __restrict__ cola,
@@ -19,30 +52,15 @@ __global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa
                                                 const fr_t* __restrict__ valb,
                                                 const fr_t* __restrict__ w, uint32_t n_rows_a,
                                                 uint32_t n_rows_b, uint32_t n, fr_t* a_out,
-                                                fr_t* b_out,
-                                                fr_t* c_out, uint32_t check, uint32_t* err) {
+                                                fr_t* b_out, fr_t* c_out, uint32_t check,
+                                                uint32_t* err) {
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  fr_t a = fr_zero(), b = fr_zero();
-  if (i < n_rows_a) {
-    for (uint32_t kx = rpa[i], ke = rpa[i + 1]; kx < ke; kx++) {
-      const fr_t wv = fr_ldg(w + cola[kx]);
-      if (check) check_canonical(wv, err);
-      a = fr_add(a, fr_mul(fr_ldg(vala + kx), wv));
-    }
-  }
-  if (i < n_rows_b) {
-    for (uint32_t kx = rpb[i], ke = rpb[i + 1]; kx < ke; kx++) {
-      const fr_t wv = fr_ldg(w + colb[kx]);
-      if (check) check_canonical(wv, err);
-      b = fr_add(b, fr_mul(fr_ldg(valb + kx), wv));
-    }
-  }
-  a = fr_canon(a);
-  b = fr_canon(b);
+  const fr_t a = i < n_rows_a ? gather_row(rpa, cola, vala, w, i, check, err) : fr_zero();
+  const fr_t b = i < n_rows_b ? gather_row(rpb, colb, valb, w, i, check, err) : fr_zero();
   fr_store(a_out + i, a);
   fr_store(b_out + i, b);
-  fr_store(c_out + i, fr_canon(fr_mul(a, b)));
+  fr_store(c_out + i, (fr_is_zero(a) || fr_is_zero(b)) ? fr_zero() : fr_canon(fr_mul(a, b)));
 }
 
 // Step 5 alone (POINTWISE_CU, g16_h_join): h = a*b - c in both encodings.

@@ -16,21 +16,22 @@
 //    shift multiplies it by g^brev(p); the 1/n of the inverse is folded into the same
 //    table (shift[p] = g^brev(p) / n), which is exact because the maps are linear.
 //  * A pass on bit b only mixes elements that differ in bit b, so passes over a range of
-//    bits [c0, c0 + KK) can run on the "slice" of 2^KK elements that agree on all other
+//    bits [c0, c0 + kk) can run on the "slice" of 2^kk elements that agree on all other
 //    bits (the six-step decomposition the NTT_CU page describes as (s0, k) batching).
 //    The lowest slice (c0 = 0) is contiguous, and the inverse's last passes and the
 //    forward's first passes both live there, so one kernel runs them back to back with
 //    the shift in between (k_ntt_mid).
 //
-// Thread mapping. A slice of 2^KK elements has 2^(KK-3) threads; in each round a thread
-// holds 8 elements in registers, those whose local indices differ only in three chosen
-// bits [P, P+3), and runs up to three radix-2 passes on them before exchanging through
-// shared memory. Local index of register e of thread t in a round at P:
-//   m = (t mod 2^P) | (e << P) | ((t >> P) << (P + 3)).
+// Inside a block every pass is a loop over butterflies, one butterfly per iteration, with
+// the slice in shared memory and a barrier between passes. The 256-bit multiply is the
+// cost that matters; keeping one copy of it per loop body keeps each kernel's hot code
+// within the instruction cache and the register count low enough for 32 warps per SM,
+// which the measured profile of an eight-element-per-thread register variant (half of all
+// issue slots lost to instruction fetch, two warps per scheduler) showed to be the limit.
 //
 // Shared memory holds each 32-byte element as two 16-byte halves in two planes, with the
-// 16-byte slot index swizzled as m ^ ((m >> 3) & 7). Every round's access pattern then
-// hits eight distinct 16-byte bank groups per quarter warp.
+// 16-byte slot index swizzled as m ^ ((m >> 3) & 7) so that runs of consecutive elements
+// and stride-2 patterns fall on distinct bank groups.
 #pragma once
 #include "fr.cuh"
 
@@ -54,7 +55,7 @@ struct SliceArgs {
   uint32_t* err;
   fr_t kscale;
   uint32_t log_n;  // k: the vector has 2^k elements
-  uint32_t kk;     // slice bits
+  uint32_t kk;     // slice bits: a block owns 2^kk elements
   uint32_t c0;     // the slice's bits are [c0, c0 + kk) of the element index
   uint32_t mode;   // SL_* flags
 };
@@ -76,10 +77,6 @@ __device__ __forceinline__ fr_t sm_get(const uint4* sm, uint32_t half, uint32_t 
   return a;
 }
 
-__device__ __forceinline__ uint32_t local_index(uint32_t t, uint32_t e, uint32_t P) {
-  return (t & ((1u << P) - 1u)) | (e << P) | ((t >> P) << (P + 3u));
-}
-
 __device__ __forceinline__ uint32_t bitrev(uint32_t x, uint32_t bits) {
   return bits == 0u ? 0u : (__brev(x) >> (32u - bits));
 }
@@ -88,206 +85,109 @@ __device__ __forceinline__ void check_canonical(const fr_t& x, uint32_t* err) {
   if (!fr_is_canonical(x)) atomicOr(err, 1u);
 }
 
-// Twiddle table index of the butterfly whose lower element is register e, for the pass
-// on slice bit lb = P + q (element bit b = c0 + lb): j = (element index) mod 2^b
-// = low + ((m mod 2^lb) << c0), index j * 2^(k - 1 - b).
-__device__ __forceinline__ uint32_t tw_index(uint32_t t, uint32_t e, uint32_t q, uint32_t P,
-                                             uint32_t low, uint32_t c0, uint32_t k) {
-  const uint32_t mmod = (t & ((1u << P) - 1u)) | ((e & ((1u << q) - 1u)) << P);
-  const uint32_t j = low + (mmod << c0);
-  return j << (k - 1u - c0 - P - q);
+// Threads of a slice kernel: one per butterfly up to 256.
+constexpr uint32_t kSliceThreads = 256;
+
+// Butterfly of the pass on slice bit lb: index bf in [0, 2^(kk-1)) -> lower element lo,
+// upper element lo + 2^lb, and the twiddle table index of the element bit c0 + lb:
+// j = (element index of lo) mod 2^(c0+lb) = low + ((lo mod 2^lb) << c0), times
+// 2^(k - 1 - c0 - lb).
+struct Bfly {
+  uint32_t lo, hi, tw;
+};
+
+__device__ __forceinline__ Bfly bfly_at(uint32_t bf, uint32_t lb, uint32_t low, uint32_t c0,
+                                        uint32_t k) {
+  Bfly b;
+  const uint32_t j = bf & ((1u << lb) - 1u);
+  b.lo = ((bf >> lb) << (lb + 1u)) | j;
+  b.hi = b.lo + (1u << lb);
+  b.tw = (low + (j << c0)) << (k - 1u - c0 - lb);
+  return b;
 }
 
-// Decimation-in-frequency passes on register bits q = qb, qb-1, ..., 0 of a round at P.
-__device__ __forceinline__ void dif_round(fr_t (&x)[8], const fr_t* __restrict__ tw, uint32_t t,
-                                          uint32_t P, int qb, uint32_t low, uint32_t c0,
-                                          uint32_t k) {
-#pragma unroll
-  for (int q = 2; q >= 0; q--) {
-    if (q > qb) continue;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-      if (e & (1 << q)) continue;
-      const int f = e | (1 << q);
-      const fr_t w = fr_ldg(tw + tw_index(t, e, q, P, low, c0, k));
-      const fr_t u = x[e];
-      x[e] = fr_add(u, x[f]);
-      x[f] = fr_mul(fr_sub(u, x[f]), w);
-    }
+// One decimation-in-frequency pass over the slice in shared memory, then a barrier.
+// When the pass is on element bit 0 every twiddle is 1 and the multiply is skipped.
+__device__ __forceinline__ void dif_pass(uint4* sm, uint32_t size, const fr_t* __restrict__ tw,
+                                         uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
+  const bool unit = (c0 + lb) == 0u;
+  for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
+    const Bfly b = bfly_at(bf, lb, low, c0, k);
+    const fr_t u = sm_get(sm, size, b.lo), v = sm_get(sm, size, b.hi);
+    fr_t d = fr_sub(u, v);
+    sm_put(sm, size, b.lo, fr_add(u, v));
+    if (!unit) d = fr_mul(d, fr_ldg(tw + b.tw));
+    sm_put(sm, size, b.hi, d);
   }
+  __syncthreads();
 }
 
-// Decimation-in-time passes on register bits q = qa, ..., 2 of a round at P.
-__device__ __forceinline__ void dit_round(fr_t (&x)[8], const fr_t* __restrict__ tw, uint32_t t,
-                                          uint32_t P, int qa, uint32_t low, uint32_t c0,
-                                          uint32_t k) {
-#pragma unroll
-  for (int q = 0; q <= 2; q++) {
-    if (q < qa) continue;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-      if (e & (1 << q)) continue;
-      const int f = e | (1 << q);
-      const fr_t w = fr_ldg(tw + tw_index(t, e, q, P, low, c0, k));
-      const fr_t v = fr_mul(x[f], w);
-      const fr_t u = x[e];
-      x[e] = fr_add(u, v);
-      x[f] = fr_sub(u, v);
-    }
+// One decimation-in-time pass, then a barrier.
+__device__ __forceinline__ void dit_pass(uint4* sm, uint32_t size, const fr_t* __restrict__ tw,
+                                         uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
+  const bool unit = (c0 + lb) == 0u;
+  for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
+    const Bfly b = bfly_at(bf, lb, low, c0, k);
+    fr_t v = sm_get(sm, size, b.hi);
+    if (!unit) v = fr_mul(v, fr_ldg(tw + b.tw));
+    const fr_t u = sm_get(sm, size, b.lo);
+    sm_put(sm, size, b.lo, fr_add(u, v));
+    sm_put(sm, size, b.hi, fr_sub(u, v));
   }
+  __syncthreads();
 }
 
-// The round at P = 0 of a contiguous slice (c0 = 0): the butterfly index j = e mod 2^q
-// is known at compile time, and j = 0 means the twiddle is 1 and the multiply is skipped.
-__device__ __forceinline__ void dif_round_p0(fr_t (&x)[8], const fr_t* __restrict__ tw, int qb,
-                                             uint32_t k) {
-#pragma unroll
-  for (int q = 2; q >= 0; q--) {
-    if (q > qb) continue;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-      if (e & (1 << q)) continue;
-      const int f = e | (1 << q);
-      const int j = e & ((1 << q) - 1);
-      const fr_t u = x[e];
-      x[e] = fr_add(u, x[f]);
-      if (j == 0) {
-        x[f] = fr_sub(u, x[f]);
-      } else {
-        const fr_t w = fr_ldg(tw + ((uint32_t)j << (k - 1u - (uint32_t)q)));
-        x[f] = fr_mul(fr_sub(u, x[f]), w);
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void dit_round_p0(fr_t (&x)[8], const fr_t* __restrict__ tw, int qa,
-                                             uint32_t k) {
-#pragma unroll
-  for (int q = 0; q <= 2; q++) {
-    if (q < qa) continue;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-      if (e & (1 << q)) continue;
-      const int f = e | (1 << q);
-      const int j = e & ((1 << q) - 1);
-      fr_t v = x[f];
-      if (j != 0) v = fr_mul(v, fr_ldg(tw + ((uint32_t)j << (k - 1u - (uint32_t)q))));
-      const fr_t u = x[e];
-      x[e] = fr_add(u, v);
-      x[f] = fr_sub(u, v);
-    }
-  }
-}
-
-// Rounds of a slice of kk bits. Decimation in frequency runs the bits from the top:
-// full rounds at P = kk-3, kk-6, ..., then (kk mod 3 != 0) a partial round at P = 0 on
-// bits kk mod 3 - 1 .. 0. Decimation in time runs from the bottom: full rounds at
-// P = 0, 3, ..., then a partial round at P = kk - 3 on its top kk mod 3 bits.
-__device__ __forceinline__ uint32_t dif_round_P(uint32_t r, uint32_t kk) {
-  return (r < kk / 3u) ? kk - 3u * (r + 1u) : 0u;
-}
-__device__ __forceinline__ int dif_round_qb(uint32_t r, uint32_t kk) {
-  return (r < kk / 3u) ? 2 : (int)(kk % 3u) - 1;
-}
-__device__ __forceinline__ uint32_t dit_round_P(uint32_t r, uint32_t kk) {
-  return (r < kk / 3u) ? 3u * r : kk - 3u;
-}
-__device__ __forceinline__ int dit_round_qa(uint32_t r, uint32_t kk) {
-  return (r < kk / 3u) ? 0 : 3 - (int)(kk % 3u);
+// Block s of a strided slice kernel owns low = s mod 2^c0, high = s >> c0 and the
+// elements low + (m << c0) + (high << (c0 + kk)), m < 2^kk.
+__device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t kk) {
+  return (size_t)(s & ((1u << c0) - 1u)) + ((size_t)(s >> c0) << (c0 + kk));
 }
 
 // ---------------------------------------------------------------------------------------
 // k_ntt_dif: decimation-in-frequency passes over slice bits [c0, c0 + kk) of vector
 // blockIdx.y, src -> dst (in place when equal: every block reads its whole slice before
-// it writes). Block s owns low = s mod 2^c0, high = s >> c0, elements
-// low + (m << c0) + (high << (c0 + kk)). Launch: grid (n >> kk, vectors), block
-// 2^(kk-3), dynamic shared memory 2^kk * 32 bytes.
-__global__ void __launch_bounds__(256) k_ntt_dif(const __grid_constant__ SliceArgs p) {
+// it writes). Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), dynamic shared
+// memory 2^kk * 32 bytes.
+__global__ void __launch_bounds__(kSliceThreads) k_ntt_dif(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
-  const uint32_t t = threadIdx.x, kk = p.kk, c0 = p.c0, k = p.log_n;
-  const uint32_t half = 1u << kk;
-  const uint32_t s = blockIdx.x, v = blockIdx.y;
-  const uint32_t low = s & ((1u << c0) - 1u);
-  const size_t base = low + ((size_t)(s >> c0) << (c0 + kk));
-  const fr_t* src = p.src[v];
-  fr_t* dst = p.dst[v];
-  const uint32_t rounds = (kk + 2u) / 3u;
-  fr_t x[8];
-  for (uint32_t r = 0; r < rounds; r++) {
-    const uint32_t P = dif_round_P(r, kk);
-    if (r == 0) {
-#pragma unroll
-      for (int e = 0; e < 8; e++) {
-        x[e] = fr_load(src + base + ((size_t)local_index(t, e, P) << c0));
-        if (p.mode & SL_CHECK) check_canonical(x[e], p.err);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; e++) x[e] = sm_get(sm, half, local_index(t, e, P));
-    }
-    dif_round(x, p.tw, t, P, dif_round_qb(r, kk), low, c0, k);
-    if (r + 1 == rounds) {
-#pragma unroll
-      for (int e = 0; e < 8; e++) fr_store(dst + base + ((size_t)local_index(t, e, P) << c0), x[e]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; e++) sm_put(sm, half, local_index(t, e, P), x[e]);
-      __syncthreads();
-    }
+  const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
+  const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
+  const size_t base = slice_base(blockIdx.x, c0, kk);
+  const fr_t* src = p.src[blockIdx.y];
+  fr_t* dst = p.dst[blockIdx.y];
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+    const fr_t x = fr_load(src + base + ((size_t)m << c0));
+    if (p.mode & SL_CHECK) check_canonical(x, p.err);
+    sm_put(sm, size, m, x);
   }
+  __syncthreads();
+  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, size, p.tw, (uint32_t)lb, low, c0, k);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+    fr_store(dst + base + ((size_t)m << c0), sm_get(sm, size, m));
 }
 
 // ---------------------------------------------------------------------------------------
 // k_ntt_mid: on the contiguous slice of 2^kk elements starting at blockIdx.x << kk of
-// vector blockIdx.y, the inverse transform's decimation-in-frequency passes on bits
+// vector blockIdx.y: the inverse transform's decimation-in-frequency passes on bits
 // kk-1 .. 0 (twiddles p.tw), the shift by scale_tab[position] (g^brev(position) / n),
 // then the forward transform's decimation-in-time passes on bits 0 .. kk-1 (twiddles
-// p.tw2). In place. Launch: grid (n >> kk, vectors), block 2^(kk-3), shared 2^kk * 32.
-__global__ void __launch_bounds__(256) k_ntt_mid(const __grid_constant__ SliceArgs p) {
+// p.tw2). In place. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
+// 2^kk * 32 bytes.
+__global__ void __launch_bounds__(kSliceThreads) k_ntt_mid(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
-  const uint32_t t = threadIdx.x, kk = p.kk, k = p.log_n;
-  const uint32_t half = 1u << kk;
+  const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
   fr_t* vec = p.dst[blockIdx.y];
-  const uint32_t rounds = (kk + 2u) / 3u;
-  fr_t x[8];
-  for (uint32_t r = 0; r < rounds; r++) {
-    const uint32_t P = dif_round_P(r, kk);
-    if (r == 0) {
-#pragma unroll
-      for (int e = 0; e < 8; e++) x[e] = fr_load(vec + base + local_index(t, e, P));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; e++) x[e] = sm_get(sm, half, local_index(t, e, P));
-    }
-    if (r + 1 < rounds) {
-      dif_round(x, p.tw, t, P, dif_round_qb(r, kk), 0u, 0u, k);
-#pragma unroll
-      for (int e = 0; e < 8; e++) sm_put(sm, half, local_index(t, e, P), x[e]);
-      __syncthreads();
-    } else {
-      // P == 0: finish the inverse, shift, start the forward on the same registers.
-      dif_round_p0(x, p.tw, dif_round_qb(r, kk), k);
-#pragma unroll
-      for (int e = 0; e < 8; e++) x[e] = fr_mul(x[e], fr_ldg(p.scale_tab + base + local_index(t, e, 0u)));
-      dit_round_p0(x, p.tw2, 0, k);
-    }
-  }
-  // decimation in time, rounds 1 .. rounds-1 (round 0 ran above)
-  for (uint32_t r = 1; r < rounds; r++) {
-    const uint32_t Pprev = dit_round_P(r - 1u, kk);
-#pragma unroll
-    for (int e = 0; e < 8; e++) sm_put(sm, half, local_index(t, e, Pprev), x[e]);
-    __syncthreads();
-    const uint32_t P = dit_round_P(r, kk);
-#pragma unroll
-    for (int e = 0; e < 8; e++) x[e] = sm_get(sm, half, local_index(t, e, P));
-    dit_round(x, p.tw2, t, P, dit_round_qa(r, kk), 0u, 0u, k);
-  }
-  const uint32_t Plast = dit_round_P(rounds - 1u, kk);
-#pragma unroll
-  for (int e = 0; e < 8; e++) fr_store(vec + base + local_index(t, e, Plast), x[e]);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+    sm_put(sm, size, m, fr_load(vec + base + m));
+  __syncthreads();
+  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, size, p.tw, (uint32_t)lb, 0u, 0u, k);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+    sm_put(sm, size, m, fr_mul(sm_get(sm, size, m), fr_ldg(p.scale_tab + base + m)));
+  __syncthreads();
+  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw2, lb, 0u, 0u, k);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+    fr_store(vec + base + m, sm_get(sm, size, m));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -298,54 +198,40 @@ __global__ void __launch_bounds__(256) k_ntt_mid(const __grid_constant__ SliceAr
 //   stored to dst[0], dst[1], and at c's store every thread re-reads the a and b values
 //   it stored itself and writes h = a*b - c to h_mont and from_mont(h) to h_std
 //   (the POINTWISE_CU join fused into the last transform's store).
-// Launch: grid (n >> kk, vectors or 1 with SL_JOIN), block 2^(kk-3), shared 2^kk * 32.
-__global__ void __launch_bounds__(256) k_ntt_dit(const __grid_constant__ SliceArgs p) {
+// Launch: grid (n >> kk, vectors or 1 with SL_JOIN), block min(2^(kk-1), 256), shared
+// 2^kk * 32 bytes.
+__global__ void __launch_bounds__(kSliceThreads) k_ntt_dit(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
-  const uint32_t t = threadIdx.x, kk = p.kk, c0 = p.c0, k = p.log_n;
-  const uint32_t half = 1u << kk;
-  const uint32_t s = blockIdx.x;
-  const uint32_t low = s & ((1u << c0) - 1u);
-  const size_t base = low + ((size_t)(s >> c0) << (c0 + kk));
-  const uint32_t rounds = (kk + 2u) / 3u;
+  const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
+  const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
+  const size_t base = slice_base(blockIdx.x, c0, kk);
   const bool join = (p.mode & SL_JOIN) != 0u;
   const uint32_t nvec = join ? 3u : 1u;
   for (uint32_t vi = 0; vi < nvec; vi++) {
     const uint32_t v = join ? vi : blockIdx.y;
     const fr_t* src = p.src[v];
     fr_t* dst = p.dst[v];
-    fr_t x[8];
-    for (uint32_t r = 0; r < rounds; r++) {
-      const uint32_t P = dit_round_P(r, kk);
-      if (r == 0) {
-        if (vi > 0) __syncthreads();  // the previous vector's last shared-memory reads
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = fr_load(src + base + ((size_t)local_index(t, e, P) << c0));
+    if (vi > 0) __syncthreads();  // the previous vector's last shared-memory reads
+    for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+      sm_put(sm, size, m, fr_load(src + base + ((size_t)m << c0)));
+    __syncthreads();
+    for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw, lb, low, c0, k);
+    for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+      const size_t i = base + ((size_t)m << c0);
+      const fr_t x = sm_get(sm, size, m);
+      if (join && v == 2u) {
+        const fr_t a = fr_load(p.dst[0] + i);
+        const fr_t b = fr_load(p.dst[1] + i);
+        const fr_t h = fr_canon(fr_sub(fr_mul(a, b), x));
+        fr_store(p.h_mont + i, h);
+        fr_store(p.h_std + i, fr_from_mont(h));
+      } else if (join) {
+        fr_store(dst + i, x);
       } else {
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = sm_get(sm, half, local_index(t, e, P));
-      }
-      dit_round(x, p.tw, t, P, dit_round_qa(r, kk), low, c0, k);
-      if (r + 1 < rounds) {
-#pragma unroll
-        for (int e = 0; e < 8; e++) sm_put(sm, half, local_index(t, e, P), x[e]);
-        __syncthreads();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-          const size_t i = base + ((size_t)local_index(t, e, P) << c0);
-          if (join && v == 2u) {
-            const fr_t a = fr_load(p.dst[0] + i);
-            const fr_t b = fr_load(p.dst[1] + i);
-            const fr_t h = fr_canon(fr_sub(fr_mul(a, b), x[e]));
-            fr_store(p.h_mont + i, h);
-            fr_store(p.h_std + i, fr_from_mont(h));
-          } else {
-            fr_t y = x[e];
-            if (p.mode & SL_SCALE_TABLE) y = fr_mul(y, fr_ldg(p.scale_tab + i));
-            if (p.mode & SL_SCALE_CONST) y = fr_mul(y, p.kscale);
-            fr_store(dst + i, join ? y : fr_canon(y));
-          }
-        }
+        fr_t y = x;
+        if (p.mode & SL_SCALE_TABLE) y = fr_mul(y, fr_ldg(p.scale_tab + i));
+        if (p.mode & SL_SCALE_CONST) y = fr_mul(y, p.kscale);
+        fr_store(dst + i, fr_canon(y));
       }
     }
   }
@@ -357,36 +243,23 @@ __global__ void __launch_bounds__(256) k_ntt_dit(const __grid_constant__ SliceAr
 // src[brev(i)] (the bit-reversal permutation absorbed into the load, as on the NTT_CU
 // page), scaled by scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and
 // the result goes to dst (out of place: a block reads other blocks' elements).
-// Launch: grid (n >> kk), block 2^(kk-3), shared 2^kk * 32.
-__global__ void __launch_bounds__(256) k_ntt_brev(const __grid_constant__ SliceArgs p) {
+// Launch: grid (n >> kk), block min(2^(kk-1), 256), shared 2^kk * 32 bytes.
+__global__ void __launch_bounds__(kSliceThreads) k_ntt_brev(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
-  const uint32_t t = threadIdx.x, kk = p.kk, k = p.log_n;
-  const uint32_t half = 1u << kk;
+  const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
-  const uint32_t rounds = (kk + 2u) / 3u;
-  fr_t x[8];
-#pragma unroll
-  for (int e = 0; e < 8; e++) {
-    const uint32_t j = bitrev((uint32_t)base + local_index(t, e, 0u), k);
-    x[e] = fr_load(p.src[0] + j);
-    if (p.mode & SL_CHECK) check_canonical(x[e], p.err);
-    if (p.mode & SL_SCALE_TABLE) x[e] = fr_mul(x[e], fr_ldg(p.scale_tab + j));
-    if (p.mode & SL_SCALE_CONST) x[e] = fr_mul(x[e], p.kscale);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+    const uint32_t j = bitrev((uint32_t)base + m, k);
+    fr_t x = fr_load(p.src[0] + j);
+    if (p.mode & SL_CHECK) check_canonical(x, p.err);
+    if (p.mode & SL_SCALE_TABLE) x = fr_mul(x, fr_ldg(p.scale_tab + j));
+    if (p.mode & SL_SCALE_CONST) x = fr_mul(x, p.kscale);
+    sm_put(sm, size, m, x);
   }
-  dit_round_p0(x, p.tw, dit_round_qa(0u, kk), k);
-  for (uint32_t r = 1; r < rounds; r++) {
-    const uint32_t Pprev = dit_round_P(r - 1u, kk);
-#pragma unroll
-    for (int e = 0; e < 8; e++) sm_put(sm, half, local_index(t, e, Pprev), x[e]);
-    __syncthreads();
-    const uint32_t P = dit_round_P(r, kk);
-#pragma unroll
-    for (int e = 0; e < 8; e++) x[e] = sm_get(sm, half, local_index(t, e, P));
-    dit_round(x, p.tw, t, P, dit_round_qa(r, kk), 0u, 0u, k);
-  }
-  const uint32_t Plast = dit_round_P(rounds - 1u, kk);
-#pragma unroll
-  for (int e = 0; e < 8; e++) fr_store(p.dst[0] + base + local_index(t, e, Plast), x[e]);
+  __syncthreads();
+  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw, lb, 0u, 0u, k);
+  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+    fr_store(p.dst[0] + base + m, sm_get(sm, size, m));
 }
 
 }  // namespace g3h
