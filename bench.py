@@ -32,24 +32,39 @@ METRIC = "Groth16 H computations/s at 2^18"
 UNIT = "H/s"
 LOG_N = 18
 WORKLOAD = "groth16_h_bn254_2^18"
-# IMAD-class operations per Montgomery multiply (64 + 64 wide 32x32 products, 8 low
-# products) and per Montgomery reduction (from_mont).
-OPS_PER_MM = 136
-OPS_PER_FROM_MONT = 72
+# Integer multiply-add work in 32-bit IMAD results: a 256-bit Montgomery multiply takes
+# 64 + 64 full 32x32 -> 64-bit products (two IMAD results each: the low and the high
+# word) and 8 low-only products; a Montgomery reduction (from_mont) 64 full and 8 low.
+OPS_PER_MM = 2 * 128 + 8
+OPS_PER_FROM_MONT = 2 * 64 + 8
 SM_COUNT = 152
-IMAD_PER_CLK_PER_SM = 64
+IMAD_PER_CLK_PER_SM = 64  # 32-bit integer multiply-add results per clock per SM
 L2_FLUSH_BYTES = 256 << 20
 
 
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default 1000; 10 for --impl reference)")
+    p.add_argument("--warmup", type=int, default=None,
+                   help="untimed warm-up steps (default 20; 1 for --impl reference)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="skip the 2^22 secondary lines")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    return p.parse_args()
+    args = p.parse_args()
+    ref = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 10 if ref else 1000
+    if args.warmup is None:
+        args.warmup = 1 if ref else 20
+    return args
+
+
+# A reference step is one whole 2^18 H by the CPU oracle (about 1.5 s on one core); when
+# the requested steps would run longer than this, the arm stops after the steps that fit
+# and reports how many it timed.
+REFERENCE_BUDGET_S = 240.0
 
 
 def dist_env():
@@ -57,6 +72,21 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def combine_ranks(local_seconds, units_per_rank, dist=None, device=None):
+    """Whole-job throughput over replicas: every rank processed units_per_rank units; the
+    job took the slowest rank's time (max over ranks). Returns (units / s, max seconds)."""
+    world = 1
+    slowest = float(local_seconds)
+    if dist is not None and dist.is_initialized():
+        import torch
+
+        world = dist.get_world_size()
+        t = torch.tensor([slowest], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        slowest = float(t.item())
+    return world * units_per_rank / slowest, slowest
 
 
 def measured_peaks():
@@ -79,8 +109,8 @@ def plan_for(k):
 
 
 def algorithmic_ops(kernel, k, nnz_a, nnz_b):
-    """Algorithmic IMAD-class operations of one launch, from the method's multiply count
-    per H: 6 (n/2) k butterfly multiplies, 3n for 1/n, 3n for the shift, n for the join
+    """Algorithmic 32-bit IMAD results of one launch, from the method's multiply count per
+    H: 6 (n/2) k butterfly multiplies, 3n for 1/n, 3n for the shift, n for the join
     product, nnz_A + nnz_B + n for the gather, and n Montgomery reductions for h_std."""
     n = 1 << k
     kk = plan_for(k)
@@ -178,18 +208,23 @@ def run_reference(args, rank, world):
     for _ in range(args.warmup):
         oracle.compute_h(LOG_N, A, B, w)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    done = 0
+    while done < args.steps:
         oracle.compute_h(LOG_N, A, B, w)
+        done += 1
+        if time.perf_counter() - t0 > REFERENCE_BUDGET_S:
+            break
     dt = time.perf_counter() - t0
-    value = args.steps / dt
+    value = done / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "steps": args.steps, "steps_timed": done, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / done,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "impl": "CPU oracle (plain C, 4x64-bit limbs)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "%d whole 2^18 H computations, one thread" % args.steps},
+                         "sample": "%d whole 2^18 H computations, one thread" % done},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -251,12 +286,9 @@ def main():
     kt = ctx.timing_read()
     ctx.timing_enable(False)
     sampler.stop()
-    step_ms = sum(a.elapsed_time(b) for a, b in evs)
-    if dist:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * args.steps / (step_ms / 1e3)
+    value, step_s = combine_ranks(sum(a.elapsed_time(b) for a, b in evs) / 1e3, args.steps,
+                                  dist, dev)
+    step_ms = step_s * 1e3
     launches = sum(v[0] for v in kt.values())
 
     # roofline of the dominant kernel: algorithmic IMAD-class ops per launch / mean time
@@ -283,9 +315,9 @@ def main():
     per_h_ops /= args.steps
     roofline = {
         "bound": "alu", "kernel": top, "achieved": achieved, "peak": peak_tops,
-        "unit": "T IMAD-ops/s", "frac": achieved / peak_tops, "traffic": traffic,
-        "peak_source": "derived: %d SMs x %d 32-bit IMAD/clk/SM x %.0f MHz" % (
-            SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
+        "unit": "T IMAD/s", "frac": achieved / peak_tops, "traffic": traffic,
+        "peak_source": "derived: %d SMs x %d 32-bit IMAD results/clk/SM x %.0f MHz; a "
+                       "32x32->64 product counts two" % (SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
         "whole_step_frac": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / peak_tops,
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()},
     }
@@ -304,11 +336,8 @@ def main():
         t = time.perf_counter()
         ctx.compute_h(wp, hmp, hsp)
         e2e_s += time.perf_counter() - t
-    if dist:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * e2e_steps / e2e_s, "unit": UNIT, "steps": e2e_steps,
+    e2e_value, e2e_s = combine_ranks(e2e_s, e2e_steps, dist, dev)
+    e2e = {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
            "h2d_bytes_per_step": int(w.nbytes), "d2h_bytes_per_step": int(2 * n * 32)}
 
     extra = {"ntt_gelem_s_2^18_in_h": 6 * n / (step_ms / args.steps * 1e-3) / 1e9}
