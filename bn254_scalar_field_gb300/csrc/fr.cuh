@@ -120,6 +120,110 @@ __device__ __forceinline__ fr_t fr_mul(const fr_t& a, const fr_t& b) {
   return c;
 }
 
+// ---------------------------------------------------------------------------------------
+// Multiplication by a constant (twiddles, shift, scale): Shoup's method (V. Shoup, NTL;
+// D. Harvey, "Faster arithmetic for number-theoretic transforms", J. Symb. Comp. 2014)
+// with beta = 2^256. For a constant w < r store w and w' = floor(w * beta / r); then for
+// any x < beta, q = floor(x * w' / beta) gives x*w - q*r in [0, 2r), since
+// x*w'/beta lies in (x*w/r - 1, x*w/r]. Here q is computed from the columns i + j >= 6 of
+// x * w' only: the dropped columns sum to less than 2^227 < beta, so q is short by at
+// most 1 and x*w - q*r lies in [0, 3r) (exact mod 2^256, as 3r < 2^256); one conditional
+// subtraction of 2r brings it to [0, 2r). With x in Montgomery form (x = X*R) and w in
+// standard form the product is the Montgomery form of X*w, so data never leaves the
+// Montgomery domain. Cost: 43 + 28 full and 16 low-only 32x32 products, against 128 full
+// and 8 low-only for a Montgomery multiply.
+struct __align__(16) fr_const_t {
+  fr_t w;   // the constant, standard form, < r
+  fr_t wp;  // floor(w * 2^256 / r)
+};
+
+// One product of a column sum (c0, c1, c2) += a*b.
+#define G3H_MAC(c0, c1, c2, a, b)                                                          \
+  asm("mad.lo.cc.u32  %0, %3, %4, %0;\n\t"                                                 \
+      "madc.hi.cc.u32 %1, %3, %4, %1;\n\t"                                                 \
+      "addc.u32       %2, %2, 0;"                                                          \
+      : "+r"(c0), "+r"(c1), "+r"(c2)                                                       \
+      : "r"(a), "r"(b))
+
+// lo = (a * b) mod 2^256, by columns.
+__device__ __forceinline__ void mul_low256(const uint32_t* a, const uint32_t* b, uint32_t* lo) {
+  uint32_t c0 = 0, c1 = 0, c2 = 0;
+#pragma unroll
+  for (int k = 0; k < 7; k++) {
+#pragma unroll
+    for (int i = 0; i <= k; i++) G3H_MAC(c0, c1, c2, a[i], b[k - i]);
+    lo[k] = c0;
+    c0 = c1;
+    c1 = c2;
+    c2 = 0;
+  }
+#pragma unroll
+  for (int i = 0; i <= 7; i++) c0 += a[i] * b[7 - i];
+  lo[7] = c0;
+}
+
+// q = words 8..15 of the sum over i + j >= 6 of a_i * b_j * 2^(32(i+j)).
+__device__ __forceinline__ void mul_high256_from6(const uint32_t* a, const uint32_t* b,
+                                                  uint32_t* q) {
+  uint32_t c0 = 0, c1 = 0, c2 = 0;
+#pragma unroll
+  for (int k = 6; k <= 14; k++) {
+#pragma unroll
+    for (int i = (k > 7 ? k - 7 : 0); i <= (k < 7 ? k : 7); i++) G3H_MAC(c0, c1, c2, a[i], b[k - i]);
+    if (k >= 8) q[k - 8] = c0;
+    c0 = c1;
+    c1 = c2;
+    c2 = 0;
+  }
+  q[7] = c0;
+}
+
+// x * w mod r in [0, 2r) for x < 2^256 and a constant given as (w, w').
+__device__ __forceinline__ fr_t fr_mul_const(const fr_t& x, const fr_t& w, const fr_t& wp) {
+  const uint32_t R[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
+  uint32_t q[8], lxw[8], lqr[8];
+  mul_high256_from6(x.v, wp.v, q);
+  mul_low256(x.v, w.v, lxw);
+  mul_low256(q, R, lqr);
+  fr_t y, d;
+  uint32_t borrow;
+  asm("sub.cc.u32  %0, %8,  %16;\n\t"
+      "subc.cc.u32 %1, %9,  %17;\n\t"
+      "subc.cc.u32 %2, %10, %18;\n\t"
+      "subc.cc.u32 %3, %11, %19;\n\t"
+      "subc.cc.u32 %4, %12, %20;\n\t"
+      "subc.cc.u32 %5, %13, %21;\n\t"
+      "subc.cc.u32 %6, %14, %22;\n\t"
+      "subc.u32    %7, %15, %23;"
+      : "=r"(y.v[0]), "=r"(y.v[1]), "=r"(y.v[2]), "=r"(y.v[3]), "=r"(y.v[4]), "=r"(y.v[5]),
+        "=r"(y.v[6]), "=r"(y.v[7])
+      : "r"(lxw[0]), "r"(lxw[1]), "r"(lxw[2]), "r"(lxw[3]), "r"(lxw[4]), "r"(lxw[5]),
+        "r"(lxw[6]), "r"(lxw[7]), "r"(lqr[0]), "r"(lqr[1]), "r"(lqr[2]), "r"(lqr[3]),
+        "r"(lqr[4]), "r"(lqr[5]), "r"(lqr[6]), "r"(lqr[7]));
+  asm("sub.cc.u32  %0, %9,  0xe0000002;\n\t"
+      "subc.cc.u32 %1, %10, 0x87c3eb27;\n\t"
+      "subc.cc.u32 %2, %11, 0xf372e122;\n\t"
+      "subc.cc.u32 %3, %12, 0x5067d090;\n\t"
+      "subc.cc.u32 %4, %13, 0x0302b0ba;\n\t"
+      "subc.cc.u32 %5, %14, 0x70a08b6d;\n\t"
+      "subc.cc.u32 %6, %15, 0xc2634053;\n\t"
+      "subc.cc.u32 %7, %16, 0x60c89ce5;\n\t"
+      "subc.u32    %8, 0, 0;"
+      : "=r"(d.v[0]), "=r"(d.v[1]), "=r"(d.v[2]), "=r"(d.v[3]), "=r"(d.v[4]), "=r"(d.v[5]),
+        "=r"(d.v[6]), "=r"(d.v[7]), "=r"(borrow)
+      : "r"(y.v[0]), "r"(y.v[1]), "r"(y.v[2]), "r"(y.v[3]), "r"(y.v[4]), "r"(y.v[5]),
+        "r"(y.v[6]), "r"(y.v[7]));
+  // borrow is 0xffffffff when y < 2r.
+#pragma unroll
+  for (int i = 0; i < 8; i++) y.v[i] = borrow ? y.v[i] : d.v[i];
+  return y;
+}
+
+// -r^{-1} mod 2^256: w' = (w * 2^256 mod r) * (-r^{-1}) mod 2^256 for w < r, because
+// w * 2^256 = w' * r + (w * 2^256 mod r) and w' < 2^256.
+#define G3H_NINV256 {0xefffffffu, 0xc2e1f593u, 0x4c6911b3u, 0x6586864bu, \
+                     0x99062391u, 0xe39a9828u, 0x0d8341b2u, 0x73f82f1du}
+
 // a + b, inputs in [0, 2r), output in [0, 2r): the sum is below 4r < 2^256, and 2r is
 // subtracted when the subtraction does not borrow.
 __device__ __forceinline__ fr_t fr_add(const fr_t& a, const fr_t& b) {
@@ -262,6 +366,17 @@ __device__ __forceinline__ bool fr_is_canonical(const fr_t& a) {
   return borrow != 0u;
 }
 
+__device__ __forceinline__ bool fr_is_zero(const fr_t& x) {
+  return (x.v[0] | x.v[1] | x.v[2] | x.v[3] | x.v[4] | x.v[5] | x.v[6] | x.v[7]) == 0u;
+}
+
+// x == 2^256 mod r, the Montgomery form of 1.
+__device__ __forceinline__ bool fr_is_mont_one(const fr_t& x) {
+  return ((x.v[0] ^ 0x4ffffffbu) | (x.v[1] ^ 0xac96341cu) | (x.v[2] ^ 0x9f60cd29u) |
+          (x.v[3] ^ 0x36fc7695u) | (x.v[4] ^ 0x7879462eu) | (x.v[5] ^ 0x666ea36fu) |
+          (x.v[6] ^ 0x9a07df2fu) | (x.v[7] ^ 0x0e0a77c1u)) == 0u;
+}
+
 // 32-byte loads and stores as two 16-byte vector accesses.
 __device__ __forceinline__ fr_t fr_load(const fr_t* p) {
   const uint4* q = reinterpret_cast<const uint4*>(p);
@@ -275,6 +390,27 @@ __device__ __forceinline__ fr_t fr_load(const fr_t* p) {
 __device__ __forceinline__ fr_t fr_ldg(const fr_t* p) {
   const uint4* q = reinterpret_cast<const uint4*>(p);
   uint4 x = __ldg(q), y = __ldg(q + 1);
+  fr_t a;
+  a.v[0] = x.x; a.v[1] = x.y; a.v[2] = x.z; a.v[3] = x.w;
+  a.v[4] = y.x; a.v[5] = y.y; a.v[6] = y.z; a.v[7] = y.w;
+  return a;
+}
+
+__device__ __forceinline__ fr_const_t fr_const_ldg(const fr_const_t* p) {
+  fr_const_t c;
+  c.w = fr_ldg(&p->w);
+  c.wp = fr_ldg(&p->wp);
+  return c;
+}
+
+__device__ __forceinline__ fr_t fr_mul_c(const fr_t& x, const fr_const_t& c) {
+  return fr_mul_const(x, c.w, c.wp);
+}
+
+// Load through L2 only (not L1): for values other blocks wrote during this kernel.
+__device__ __forceinline__ fr_t fr_ldcg(const fr_t* p) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  uint4 x = __ldcg(q), y = __ldcg(q + 1);
   fr_t a;
   a.v[0] = x.x; a.v[1] = x.y; a.v[2] = x.z; a.v[3] = x.w;
   a.v[4] = y.x; a.v[5] = y.y; a.v[6] = y.z; a.v[7] = y.w;

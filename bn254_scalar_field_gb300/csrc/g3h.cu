@@ -2,8 +2,9 @@
 //
 // Work per H computation on a domain of 2^k >= 2^6 points (two slice levels, k = lo + hi;
 // three levels for k > 22; a slice is at most 2^11 elements):
-//   k_gather                 a, b, c                       (skipped by compute_h_abc)
-//   k_ntt_dif  (3 vectors)   inverse passes on the top bits, strided slices
+//   k_ntt_dif  (3 vectors)   inverse passes on the top bits, strided slices; for
+//                            compute_h the gather forms a, b, c in its load
+//                            (compute_h_abc loads them)
 //   k_ntt_mid  (3 vectors)   inverse passes on the low bits, shift g^brev(p)/n, forward
 //                            passes on the low bits, contiguous slices
 //   k_ntt_dit  (join)        forward passes on the top bits for a, b, then c with
@@ -94,13 +95,17 @@ struct g3h_ctx {
   uint32_t *d_rpa = nullptr, *d_cola = nullptr, *d_rpb = nullptr, *d_colb = nullptr;
   fr_t *d_vala = nullptr, *d_valb = nullptr;
   fr_t* d_consts = nullptr;  // omega, omega^-1, g, g^-1, n^-1, 1 (Montgomery)
-  fr_t *d_tw_fwd = nullptr, *d_tw_inv = nullptr, *d_shift_br = nullptr;
-  fr_t *d_coset_fwd = nullptr, *d_coset_inv = nullptr;
-  fr_t* d_abc = nullptr;  // 3n scratch
+  // constant tables in the (w, w') form of the constant multiply
+  fr_const_t *d_tw_fwd = nullptr, *d_tw_inv = nullptr, *d_shift_br = nullptr;
+  fr_const_t *d_coset_fwd = nullptr, *d_coset_inv = nullptr;
+  fr_const_t* d_ninv = nullptr;  // n^-1
+  fr_t* d_abc = nullptr;  // 3n scratch: a | b | c while they are transformed
+  fr_t* d_ab_in = nullptr;  // 2n: the gather's a | b, read by the first inverse kernel
+  uint32_t* d_counters = nullptr;  // per top-level slice, for the fused join (kept zero)
   fr_t* d_stage = nullptr;
   size_t stage_elems = 0;
   uint32_t* d_err = nullptr;
-  fr_t h_consts[6];
+  fr_const_t h_ninv;  // host copy of n^-1, passed by value to kernels
   bool timing = false;
   std::vector<TimedLaunch> launches;
   std::vector<cudaEvent_t> event_pool;
@@ -118,7 +123,8 @@ int dalloc(T** p, size_t count) {
 void release(g3h_ctx* c) {
   void* bufs[] = {c->d_rpa,      c->d_cola,     c->d_rpb,      c->d_colb,        c->d_vala,
                   c->d_valb,     c->d_consts,   c->d_tw_fwd,   c->d_tw_inv,      c->d_shift_br,
-                  c->d_coset_fwd, c->d_coset_inv, c->d_abc,    c->d_stage,       c->d_err};
+                  c->d_coset_fwd, c->d_coset_inv, c->d_abc,    c->d_stage,       c->d_err,
+                  c->d_ab_in,    c->d_counters, c->d_ninv};
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
@@ -171,7 +177,7 @@ int set_smem_limits() {
   return G3H_OK;
 }
 
-int build_table(g3h_ctx* c, fr_t* tab, size_t count, int base, int scale, uint32_t brev) {
+int build_table(g3h_ctx* c, fr_const_t* tab, size_t count, int base, int scale, uint32_t brev) {
   if (count == 0) return G3H_OK;
   return run(c, "tables", [&] {
     k_pow_table<<<blocks_for(count, 256), 256, 0, c->stream>>>(tab, count, c->d_consts, base,
@@ -235,13 +241,37 @@ SliceArgs base_args(g3h_ctx* c, uint32_t flags) {
   return a;
 }
 
+int gather(g3h_ctx* c, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc, uint32_t flags);
+
 // Steps 2-5 on device vectors a, b, c -> h_mont, h_std (device). a, b, c may be the
-// context's scratch vectors.
-int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, fr_t* hm, fr_t* hs,
-             uint32_t flags) {
+// context's scratch vectors. With a witness w (device) instead, steps 1-5: the gather
+// is fused into the load of the first inverse kernel (a, b, c are then ignored).
+int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_t* w, fr_t* hm,
+             fr_t* hs, uint32_t flags) {
   const uint32_t k = c->log_n;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   const size_t n = c->n;
+  if (w && k <= kSmallMaxLog) {
+    fr_t* s3 = c->d_abc;
+    const int rc = gather(c, w, s3, s3 + n, s3 + 2 * n, flags);
+    if (rc != G3H_OK) return rc;
+    a = s3;
+    b = s3 + n;
+    cc = s3 + 2 * n;
+  } else if (w) {
+    // a and b by the gather; c = a * b is formed by the first inverse kernel at load
+    fr_t* ab = c->d_ab_in;
+    const uint32_t chk = check;
+    const int rc = run(c, "gather", [&] {
+      k_gather_ab<<<blocks_for(2 * n, 256), 256, 0, c->stream>>>(
+          c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
+          c->n_rows_b, (uint32_t)n, ab, ab + n, chk, c->d_err);
+    });
+    if (rc != G3H_OK) return rc;
+    a = ab;
+    b = ab + n;
+    cc = nullptr;
+  }
   if (k <= kSmallMaxLog) {
     return run(c, "small_quotient", [&] {
       k_small_quotient<<<1, 32, 0, c->stream>>>(a, b, cc, c->d_tw_inv, c->d_tw_fwd,
@@ -262,7 +292,8 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, fr_t* hm,
     x.tw = c->d_tw_inv;
     x.kk = pl.kk[lvl];
     x.c0 = pl.c0[lvl];
-    x.mode = (first && check) ? SL_CHECK : 0u;
+    x.mode = (first && check && !w) ? SL_CHECK : 0u;
+    if (first && w) x.mode |= SL_C_FROM_AB;
     rc = launch_slice(c, "ntt_dif", k_ntt_dif, x, 3);
   }
   if (rc != G3H_OK) return rc;
@@ -293,10 +324,11 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, fr_t* hm,
   x.kk = pl.kk[top];
   x.c0 = pl.c0[top];
   if (!(flags & G3H_UNFUSED_JOIN)) {
-    x.mode = SL_JOIN;
+    x.mode = SL_JOIN_LAST;
     x.h_mont = hm;
     x.h_std = hs;
-    return launch_slice(c, "ntt_dit_join", k_ntt_dit, x, 1);
+    x.counters = c->d_counters;
+    return launch_slice(c, "ntt_dit_join", k_ntt_dit, x, 3);
   }
   rc = launch_slice(c, "ntt_dit", k_ntt_dit, x, 3);
   if (rc != G3H_OK) return rc;
@@ -322,13 +354,13 @@ int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
     const int rc = ensure_coset_tables(c);
     if (rc != G3H_OK) return rc;
   }
-  const fr_t* tw = inverse ? c->d_tw_inv : c->d_tw_fwd;
-  const fr_t* scale_load = (!inverse && coset) ? c->d_coset_fwd : nullptr;
-  const fr_t* scale_store = (inverse && coset) ? c->d_coset_inv : nullptr;
+  const fr_const_t* tw = inverse ? c->d_tw_inv : c->d_tw_fwd;
+  const fr_const_t* scale_load = (!inverse && coset) ? c->d_coset_fwd : nullptr;
+  const fr_const_t* scale_store = (inverse && coset) ? c->d_coset_inv : nullptr;
   const bool store_const = inverse && !coset;
   if (k <= kSmallMaxLog) {
     return run(c, "small_ntt", [&] {
-      k_small_ntt<<<1, 32, 0, c->stream>>>(data, tw, scale_load, scale_store, c->h_consts[4],
+      k_small_ntt<<<1, 32, 0, c->stream>>>(data, tw, scale_load, scale_store, c->h_ninv,
                                             store_const ? 1u : 0u, k, check, c->d_err);
     });
   }
@@ -355,7 +387,7 @@ int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
         y.scale_tab = scale_store;
         y.mode = SL_SCALE_TABLE;
       } else if (store_const) {
-        y.kscale = c->h_consts[4];
+        y.kscale = c->h_ninv;
         y.mode = SL_SCALE_CONST;
       }
     }
@@ -456,11 +488,21 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
   if (rc == G3H_OK) rc = dalloc(&c->d_tw_inv, n / 2);
   if (rc == G3H_OK) rc = dalloc(&c->d_shift_br, n);
   if (rc == G3H_OK) rc = dalloc(&c->d_abc, 3 * n);
+  if (rc == G3H_OK && A) rc = dalloc(&c->d_ab_in, 2 * n);
+  const size_t n_slices = n >> plan_for(log_n).kk[plan_for(log_n).levels - 1];
+  if (rc == G3H_OK) rc = dalloc(&c->d_counters, n_slices);
+  if (rc == G3H_OK)
+    rc = cudaMemsetAsync(c->d_counters, 0, std::max<size_t>(n_slices, 1) * sizeof(uint32_t),
+                         c->stream) == cudaSuccess
+             ? G3H_OK
+             : G3H_E_CUDA;
   if (rc == G3H_OK)
     rc = run(c, "tables", [&] { k_domain<<<1, 1, 0, c->stream>>>(c->d_consts, log_n); });
   if (rc == G3H_OK) rc = build_table(c, c->d_tw_fwd, n / 2, 0, -1, 0);
   if (rc == G3H_OK) rc = build_table(c, c->d_tw_inv, n / 2, 1, -1, 0);
   if (rc == G3H_OK) rc = build_table(c, c->d_shift_br, n, 2, 4, log_n);
+  if (rc == G3H_OK) rc = dalloc(&c->d_ninv, 1);
+  if (rc == G3H_OK) rc = build_table(c, c->d_ninv, 1, 5, 4, 0);  // 1^0 * n^-1
   if (rc == G3H_OK && A) {
     c->has_csr = true;
     c->n_rows_a = A->n_rows;
@@ -469,7 +511,7 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
     if (rc == G3H_OK) rc = upload_csr(c, B, &c->d_rpb, &c->d_colb, &c->d_valb);
   }
   if (rc == G3H_OK)
-    rc = cudaMemcpyAsync(c->h_consts, c->d_consts, sizeof(c->h_consts), cudaMemcpyDeviceToHost,
+    rc = cudaMemcpyAsync(&c->h_ninv, c->d_ninv, sizeof(c->h_ninv), cudaMemcpyDeviceToHost,
                          c->stream) == cudaSuccess
              ? G3H_OK
              : G3H_E_CUDA;
@@ -490,19 +532,16 @@ int g3h_compute_h(g3h_ctx* c, const uint32_t* witness, uint32_t* h_mont, uint32_
   DeviceGuard guard(c->device);
   const size_t n = c->n;
   fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
-  if (flags & G3H_DEVICE_PTRS) {
-    int rc = gather(c, (const fr_t*)witness, s[0], s[1], s[2], flags);
-    if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], (fr_t*)h_mont, (fr_t*)h_std, flags);
-    return rc;
-  }
+  if (flags & G3H_DEVICE_PTRS)
+    return quotient(c, s[0], s[1], s[2], (const fr_t*)witness, (fr_t*)h_mont, (fr_t*)h_std,
+                    flags);
   int rc = ensure_stage(c, (size_t)c->n_wires + 2 * n);
   if (rc != G3H_OK) return rc;
   fr_t* w = c->d_stage;
   fr_t* hm = c->d_stage + c->n_wires;
   fr_t* hs = hm + n;
   rc = h2d(c, w, witness, (size_t)c->n_wires * sizeof(fr_t));
-  if (rc == G3H_OK) rc = gather(c, w, s[0], s[1], s[2], flags);
-  if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], hm, hs, flags);
+  if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], w, hm, hs, flags);
   if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
   const int rc2 = finish(c);
@@ -515,7 +554,7 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
   DeviceGuard guard(c->device);
   const size_t n = c->n;
   if (flags & G3H_DEVICE_PTRS)
-    return quotient(c, (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, (fr_t*)h_mont,
+    return quotient(c, (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, nullptr, (fr_t*)h_mont,
                     (fr_t*)h_std, flags);
   int rc = ensure_stage(c, 5 * n);
   if (rc != G3H_OK) return rc;
@@ -525,7 +564,7 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
   rc = h2d(c, in, a, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = h2d(c, in + n, b, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = h2d(c, in + 2 * n, cc, n * sizeof(fr_t));
-  if (rc == G3H_OK) rc = quotient(c, in, in + n, in + 2 * n, hm, hs, flags);
+  if (rc == G3H_OK) rc = quotient(c, in, in + n, in + 2 * n, nullptr, hm, hs, flags);
   if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
   const int rc2 = finish(c);
@@ -689,18 +728,19 @@ int g3h_timing_read(g3h_ctx* c, g3h_kernel_time* out, int max, int* count) {
 // latency-critical paths that cannot afford cudaMalloc's device-wide synchronisation.
 // The working vectors and the domain tables live in one file-scope device array of fixed
 // size, reserved on every GPU that loads this library until the process exits:
+// (in 32-byte elements; a table entry (w, w') takes two)
 //   [0, 3N)          the three working vectors a, b, c
-//   [3N, 3.5N)       forward twiddles omega^j, j < n/2
-//   [3.5N, 4N)       inverse twiddles omega^-j, j < n/2
-//   [4N, 5N)         shift table g^brev(p) / n
-//   [5N, 5N + 6)     domain constants
-// with N = 2^16, the largest domain this entry point accepts: 5N + 8 elements of 32 bytes,
-// 10 MiB. Every element of the array that a call reads was written earlier in the same
+//   [3N, 4N)         forward twiddles omega^j, j < n/2
+//   [4N, 5N)         inverse twiddles omega^-j, j < n/2
+//   [5N, 7N)         shift table g^brev(p) / n
+//   [7N, 7N + 6)     domain constants
+// with N = 2^16, the largest domain this entry point accepts: 7N + 8 elements of 32 bytes,
+// 14 MiB. Every element of the array that a call reads was written earlier in the same
 // call or by the table build for the same domain, so nothing has to start at zero.
 namespace {
 constexpr uint32_t kNoAllocMaxLog = 16;
 constexpr size_t kNoAllocN = (size_t)1 << kNoAllocMaxLog;
-constexpr size_t kNoAllocElems = 5 * kNoAllocN + 8;
+constexpr size_t kNoAllocElems = 7 * kNoAllocN + 8;
 }  // namespace
 
 static __device__ __align__(256) fr_t g3h_noalloc_scratch[kNoAllocElems];
@@ -739,10 +779,10 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
   const cudaStream_t s = (cudaStream_t)stream;
   const size_t n = (size_t)1 << log_n;
   fr_t* work = d.base;
-  fr_t* tw_fwd = d.base + 3 * kNoAllocN;
-  fr_t* tw_inv = tw_fwd + kNoAllocN / 2;
-  fr_t* shift = tw_inv + kNoAllocN / 2;
-  fr_t* consts = shift + kNoAllocN;
+  fr_const_t* tw_fwd = reinterpret_cast<fr_const_t*>(d.base + 3 * kNoAllocN);
+  fr_const_t* tw_inv = tw_fwd + kNoAllocN / 2;
+  fr_const_t* shift = tw_inv + kNoAllocN / 2;
+  fr_t* consts = reinterpret_cast<fr_t*>(shift + kNoAllocN);
   if (d.table_log != (int)log_n) {
     d.table_log = -1;
     k_domain<<<1, 1, 0, s>>>(consts, log_n);

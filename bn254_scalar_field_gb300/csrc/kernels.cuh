@@ -6,43 +6,92 @@
 namespace g3h {
 
 // ---------------------------------------------------------------------------------------
-// Step 1 (GATHER_CU, g16_gather_abc): a_i = sum over CSR row i of A.val[k] * w[A.col[k]],
-// b_i likewise, c_i = a_i * b_i, for i < n; rows at or beyond a matrix's n_rows are empty.
-// One thread per row, as on the page: the rows are short (mean 1-4 terms), ragged and
-// half empty, so a cooperative mapping would idle most lanes. Outputs are canonical.
+// Step 1, the sums only: thread t < n forms a_t from row t of A, thread n + t forms b_t
+// from row t of B; c = a * b is then formed by the first inverse kernel at load
+// (SL_C_FROM_AB). Outputs canonical. Launch: ceil(2n / 256) blocks of 256.
 //
-// Most witness values of a circuit are 0 or 1 (bits, flags, the constant wire), so a term
-// whose wire value is 0 contributes nothing and one whose value is the Montgomery form of
-// 1 contributes its coefficient unchanged; only the remaining terms take a multiply, and
-// c is only multiplied out when both a and b are non-zero. These are identities of the
-// field, so the outputs are the same canonical values.
-__device__ __forceinline__ bool fr_is_zero(const fr_t& x) {
-  return (x.v[0] | x.v[1] | x.v[2] | x.v[3] | x.v[4] | x.v[5] | x.v[6] | x.v[7]) == 0u;
+// The kernel lasts as long as its slowest warp, and a row is a chain of dependent loads
+// (column, witness value, coefficient) per term, so the longest row (95 terms in the
+// 2^18 key) would set the time alone. Rows of at most kGatherLaneTerms terms are summed
+// by their own lane; longer rows are summed by the whole warp, lanes striding over the
+// terms, then combined with a shuffle reduction. Sums are mod r in any order, so the
+// outputs are the same canonical values.
+constexpr uint32_t kGatherLaneTerms = 8;
+
+__device__ __forceinline__ fr_t gather_term(const uint32_t* __restrict__ col,
+                                            const fr_t* __restrict__ val,
+                                            const fr_t* __restrict__ w, uint32_t kx,
+                                            uint32_t check, uint32_t* err) {
+  const fr_t wv = fr_ldg(w + col[kx]);
+  if (check) check_canonical(wv, err);
+  if (fr_is_zero(wv)) return fr_zero();
+  const fr_t cv = fr_ldg(val + kx);
+  return fr_is_mont_one(wv) ? cv : fr_mul(cv, wv);
 }
 
-// 2^256 mod r: the Montgomery form of 1.
-__device__ __forceinline__ bool fr_is_mont_one(const fr_t& x) {
-  return ((x.v[0] ^ 0x4ffffffbu) | (x.v[1] ^ 0xac96341cu) | (x.v[2] ^ 0x9f60cd29u) |
-          (x.v[3] ^ 0x36fc7695u) | (x.v[4] ^ 0x7879462eu) | (x.v[5] ^ 0x666ea36fu) |
-          (x.v[6] ^ 0x9a07df2fu) | (x.v[7] ^ 0x0e0a77c1u)) == 0u;
+__device__ __forceinline__ fr_t fr_shfl_xor(const fr_t& x, int lane_mask) {
+  fr_t y;
+#pragma unroll
+  for (int j = 0; j < 8; j++) y.v[j] = __shfl_xor_sync(0xffffffffu, x.v[j], lane_mask);
+  return y;
 }
 
-__device__ __forceinline__ fr_t gather_row(const uint32_t* __restrict__ rp,
-                                           const uint32_t* __restrict__ col,
-                                           const fr_t* __restrict__ val,
-                                           const fr_t* __restrict__ w, uint32_t i,
-                                           uint32_t check, uint32_t* err) {
-  fr_t acc = fr_zero();
-  for (uint32_t kx = rp[i], ke = rp[i + 1]; kx < ke; kx++) {
-    const fr_t wv = fr_ldg(w + col[kx]);
-    if (check) check_canonical(wv, err);
-    if (fr_is_zero(wv)) continue;
-    const fr_t cv = fr_ldg(val + kx);
-    acc = fr_add(acc, fr_is_mont_one(wv) ? cv : fr_mul(cv, wv));
+__global__ void __launch_bounds__(256) k_gather_ab(const uint32_t* __restrict__ rpa,
+                                                   const uint32_t* __restrict__ cola,
+                                                   const fr_t* __restrict__ vala,
+                                                   const uint32_t* __restrict__ rpb,
+                                                   const uint32_t* __restrict__ colb,
+                                                   const fr_t* __restrict__ valb,
+                                                   const fr_t* __restrict__ w,
+                                                   uint32_t n_rows_a, uint32_t n_rows_b,
+                                                   uint32_t n, fr_t* a_out, fr_t* b_out,
+                                                   uint32_t check, uint32_t* err) {
+  // No early return: every lane takes part in the warp-wide loop below.
+  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t lane = threadIdx.x & 31u;
+  const bool is_b = t >= n;
+  const uint32_t i = is_b ? t - n : t;
+  const bool valid = t < 2u * n && i < (is_b ? n_rows_b : n_rows_a);
+  const uint32_t* rp = is_b ? rpb : rpa;
+  const uint32_t* col = is_b ? colb : cola;
+  const fr_t* val = is_b ? valb : vala;
+  uint32_t kx = 0, ke = 0;
+  if (valid) {
+    kx = rp[i];
+    ke = rp[i + 1];
   }
-  return fr_canon(acc);
+  const bool lane_row = ke - kx <= kGatherLaneTerms;
+  fr_t acc = fr_zero();
+  if (lane_row) {
+    for (; kx + 2u <= ke; kx += 2u) {
+      const fr_t x = gather_term(col, val, w, kx, check, err);
+      const fr_t y = gather_term(col, val, w, kx + 1u, check, err);
+      acc = fr_add(acc, fr_add(x, y));
+    }
+    if (kx < ke) acc = fr_add(acc, gather_term(col, val, w, kx, check, err));
+  }
+  // The warp's long rows, one at a time. The matrix is the same across a warp except at
+  // the A/B seam, so each long row carries its own matrix pointers through the shuffle.
+  uint32_t longs = __ballot_sync(0xffffffffu, !lane_row);
+  while (longs) {
+    const int src = __ffs(longs) - 1;
+    longs &= longs - 1u;
+    const uint32_t rb = __shfl_sync(0xffffffffu, kx, src);
+    const uint32_t re = __shfl_sync(0xffffffffu, ke, src);
+    const bool rb_is_b = __shfl_sync(0xffffffffu, (uint32_t)is_b, src) != 0u;
+    const uint32_t* rcol = rb_is_b ? colb : cola;
+    const fr_t* rval = rb_is_b ? valb : vala;
+    fr_t part = fr_zero();
+    for (uint32_t k = rb + lane; k < re; k += 32u)
+      part = fr_add(part, gather_term(rcol, rval, w, k, check, err));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part = fr_add(part, fr_shfl_xor(part, off));
+    if ((int)lane == src) acc = part;
+  }
+  if (t < 2u * n) fr_store((is_b ? b_out : a_out) + i, fr_canon(acc));
 }
 
+// Step 1 alone (GATHER_CU, g16_gather_abc; gather_row in ntt.cuh). Outputs are canonical.
 // Launch: ceil(n / 256) blocks of 256.
 __global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa,
                                                 const uint32_t* __restrict__ cola,
@@ -60,7 +109,7 @@ __global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa
   const fr_t b = i < n_rows_b ? gather_row(rpb, colb, valb, w, i, check, err) : fr_zero();
   fr_store(a_out + i, a);
   fr_store(b_out + i, b);
-  fr_store(c_out + i, (fr_is_zero(a) || fr_is_zero(b)) ? fr_zero() : fr_canon(fr_mul(a, b)));
+  fr_store(c_out + i, gather_c(a, b));
 }
 
 // Step 5 alone (POINTWISE_CU, g16_h_join): h = a*b - c in both encodings.
@@ -104,9 +153,9 @@ constexpr uint32_t kSmallMaxLog = 5;
 // shift_br[p] = g^brev(p) / n, decimation-in-time forward (tw_fwd), join.
 // Launch: 1 block of 32 threads.
 __global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t* b,
-                                                       const fr_t* c, const fr_t* tw_inv,
-                                                       const fr_t* tw_fwd,
-                                                       const fr_t* shift_br, fr_t* h_mont,
+                                                       const fr_t* c, const fr_const_t* tw_inv,
+                                                       const fr_const_t* tw_fwd,
+                                                       const fr_const_t* shift_br, fr_t* h_mont,
                                                        fr_t* h_std, uint32_t k,
                                                        uint32_t check, uint32_t* err) {
   __shared__ fr_t s[3][1u << kSmallMaxLog];
@@ -127,13 +176,13 @@ __global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t
         const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
         const fr_t u = s[v][lo], w = s[v][hi];
         s[v][lo] = fr_add(u, w);
-        s[v][hi] = fr_mul(fr_sub(u, w), tw_inv[j << (k - 1u - bit)]);
+        s[v][hi] = fr_mul_c(fr_sub(u, w), tw_inv[j << (k - 1u - bit)]);
       }
     }
     __syncthreads();
   }
   for (uint32_t v = 0; v < 3; v++)
-    for (uint32_t i = tid; i < n; i += blockDim.x) s[v][i] = fr_mul(s[v][i], shift_br[i]);
+    for (uint32_t i = tid; i < n; i += blockDim.x) s[v][i] = fr_mul_c(s[v][i], shift_br[i]);
   __syncthreads();
   for (uint32_t bit = 0; bit < k; bit++) {
     for (uint32_t v = 0; v < 3; v++) {
@@ -141,7 +190,7 @@ __global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t
         const uint32_t j = f & ((1u << bit) - 1u);
         const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
         const fr_t u = s[v][lo];
-        const fr_t w = fr_mul(s[v][hi], tw_fwd[j << (k - 1u - bit)]);
+        const fr_t w = fr_mul_c(s[v][hi], tw_fwd[j << (k - 1u - bit)]);
         s[v][lo] = fr_add(u, w);
         s[v][hi] = fr_sub(u, w);
       }
@@ -159,9 +208,9 @@ __global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t
 // data[brev(p)] (times scale_load[brev(p)] if given), decimation-in-time passes with tw,
 // stores times scale_store[p] if given, else times kscale if given.
 // Launch: 1 block of 32 threads.
-__global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_t* tw,
-                                                  const fr_t* scale_load,
-                                                  const fr_t* scale_store, fr_t kscale,
+__global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_const_t* tw,
+                                                  const fr_const_t* scale_load,
+                                                  const fr_const_t* scale_store, fr_const_t kscale,
                                                   uint32_t use_kscale, uint32_t k,
                                                   uint32_t check, uint32_t* err) {
   __shared__ fr_t s[1u << kSmallMaxLog];
@@ -170,7 +219,7 @@ __global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_t* tw,
     const uint32_t j = bitrev(i, k);
     fr_t x = fr_load(data + j);
     if (check) check_canonical(x, err);
-    if (scale_load) x = fr_mul(x, scale_load[j]);
+    if (scale_load) x = fr_mul_c(x, scale_load[j]);
     s[i] = x;
   }
   __syncthreads();
@@ -179,7 +228,7 @@ __global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_t* tw,
       const uint32_t j = f & ((1u << bit) - 1u);
       const uint32_t lo = ((f >> bit) << (bit + 1u)) | j, hi = lo + (1u << bit);
       const fr_t u = s[lo];
-      const fr_t w = fr_mul(s[hi], tw[j << (k - 1u - bit)]);
+      const fr_t w = fr_mul_c(s[hi], tw[j << (k - 1u - bit)]);
       s[lo] = fr_add(u, w);
       s[hi] = fr_sub(u, w);
     }
@@ -187,8 +236,8 @@ __global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_t* tw,
   }
   for (uint32_t i = tid; i < n; i += blockDim.x) {
     fr_t x = s[i];
-    if (scale_store) x = fr_mul(x, scale_store[i]);
-    else if (use_kscale) x = fr_mul(x, kscale);
+    if (scale_store) x = fr_mul_c(x, scale_store[i]);
+    else if (use_kscale) x = fr_mul_c(x, kscale);
     fr_store(data + i, fr_canon(x));
   }
 }
@@ -259,16 +308,22 @@ __global__ void k_domain(fr_t* out, uint32_t k) {
   out[5] = fr_one_mont();
 }
 
-// tab[i] = scale * base^(bit-reversed i if brev_bits else i), i < count; base and scale
-// are indices into the domain constants (scale < 0: none). Launch: ceil(count/256) x 256.
-__global__ void k_pow_table(fr_t* tab, size_t count, const fr_t* consts, int base_idx,
+// tab[i] = the constant scale * base^(bit-reversed i if brev_bits else i), i < count, in
+// the (w, w') form of the constant multiply; base and scale are indices into the domain
+// constants (scale < 0: none). The power is formed in Montgomery form x = w*R mod r, then
+// w = from_mont(x) and w' = x * (-r^-1) mod 2^256. Launch: ceil(count/256) x 256.
+__global__ void k_pow_table(fr_const_t* tab, size_t count, const fr_t* consts, int base_idx,
                             int scale_idx, uint32_t brev_bits) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count) return;
   const uint32_t e = brev_bits ? bitrev((uint32_t)i, brev_bits) : (uint32_t)i;
   fr_t x = fr_pow_u32(consts[base_idx], e);
   if (scale_idx >= 0) x = fr_canon(fr_mul(x, consts[scale_idx]));
-  tab[i] = x;
+  const uint32_t ninv[8] = G3H_NINV256;
+  fr_const_t c;
+  c.w = fr_from_mont(x);
+  mul_low256(x.v, ninv, c.wp.v);
+  tab[i] = c;
 }
 
 }  // namespace g3h

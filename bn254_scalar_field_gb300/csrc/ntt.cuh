@@ -22,6 +22,9 @@
 //    forward's first passes both live there, so one kernel runs them back to back with
 //    the shift in between (k_ntt_mid).
 //
+// Every multiplication here is by a table constant (twiddle, shift, scale), so it uses
+// the constant multiply of fr.cuh (Shoup's method, tables of (w, w') pairs).
+//
 // Inside a block every pass is a loop over butterflies, one butterfly per iteration, with
 // the slice in shared memory and a barrier between passes. The 256-bit multiply is the
 // cost that matters; keeping one copy of it per loop body keeps each kernel's hot code
@@ -30,8 +33,8 @@
 // issue slots lost to instruction fetch, two warps per scheduler) showed to be the limit.
 //
 // Shared memory holds each 32-byte element as two 16-byte halves in two planes, with the
-// 16-byte slot index swizzled as m ^ ((m >> 3) & 7) so that runs of consecutive elements
-// and stride-2 patterns fall on distinct bank groups.
+// 16-byte slot index swizzled (swz below) so that every access pattern of the passes
+// falls on distinct bank groups.
 #pragma once
 #include "fr.cuh"
 
@@ -42,25 +45,35 @@ enum : uint32_t {
   SL_SCALE_TABLE = 2u,  // scale by scale_tab (see each kernel)
   SL_SCALE_CONST = 4u,  // scale by kscale
   SL_JOIN = 8u,         // k_ntt_dit: vectors 0, 1, 2 are a, b, c; write h = a*b - c
+  SL_C_FROM_AB = 16u,   // k_ntt_dif: vector 2 (c) is not loaded but formed as
+                        // src[0][i] * src[1][i] (the gather's C = A o B) at load
+  SL_JOIN_LAST = 32u,   // k_ntt_dit: vectors 0, 1, 2 (grid.y) are a, b, c; the last of a
+                        // slice's three blocks to finish writes h for that slice
 };
 
 struct SliceArgs {
   const fr_t* src[3];
   fr_t* dst[3];
-  const fr_t* tw;         // twiddles of the passes (forward or inverse table, n/2 entries)
-  const fr_t* tw2;        // k_ntt_mid: forward twiddles for its decimation-in-time half
-  const fr_t* scale_tab;  // per-kernel scale table (n entries)
+  const fr_const_t* tw;         // twiddles of the passes (forward or inverse, n/2 entries)
+  const fr_const_t* tw2;        // k_ntt_mid: forward twiddles for its decimation-in-time half
+  const fr_const_t* scale_tab;  // per-kernel scale table (n entries)
   fr_t* h_mont;
   fr_t* h_std;
   uint32_t* err;
-  fr_t kscale;
+  fr_const_t kscale;
   uint32_t log_n;  // k: the vector has 2^k elements
   uint32_t kk;     // slice bits: a block owns 2^kk elements
   uint32_t c0;     // the slice's bits are [c0, c0 + kk) of the element index
   uint32_t mode;   // SL_* flags
+  uint32_t* counters;  // SL_JOIN_LAST: one zeroed counter per slice, left zeroed
 };
 
-__device__ __forceinline__ uint32_t swz(uint32_t m) { return m ^ ((m >> 3) & 7u); }
+// 16-byte slot of element m's half: the low three bits (the bank group of a 16-byte
+// access) are XORed with a fold of the higher bits, so that eight lanes at element
+// strides 1, 2, 4, ..., 128 land on eight distinct bank groups.
+__device__ __forceinline__ uint32_t swz(uint32_t m) {
+  return m ^ (((m >> 3) ^ (m >> 6) ^ (m >> 9)) & 7u);
+}
 
 __device__ __forceinline__ void sm_put(uint4* sm, uint32_t half, uint32_t m, const fr_t& x) {
   const uint32_t s = swz(m);
@@ -85,8 +98,49 @@ __device__ __forceinline__ void check_canonical(const fr_t& x, uint32_t* err) {
   if (!fr_is_canonical(x)) atomicOr(err, 1u);
 }
 
-// Threads of a slice kernel: one per butterfly up to 256.
-constexpr uint32_t kSliceThreads = 256;
+// ---------------------------------------------------------------------------------------
+// Step 1 (GATHER_CU, g16_gather_abc): a_i = sum over CSR row i of A.val[k] * w[A.col[k]],
+// b_i likewise, c_i = a_i * b_i; one thread per row, as on the page (rows are short,
+// ragged and half empty).
+//
+// Most witness values of a circuit are 0 or 1 (bits, flags, the constant wire), so a term
+// whose wire value is 0 contributes nothing and one whose value is the Montgomery form of
+// 1 contributes its coefficient unchanged; only the remaining terms take a multiply, and
+// c is only multiplied out when both a and b are non-zero. These are identities of the
+// field, so the outputs are the same canonical values.
+__device__ __forceinline__ fr_t gather_row(const uint32_t* __restrict__ rp,
+                                           const uint32_t* __restrict__ col,
+                                           const fr_t* __restrict__ val,
+                                           const fr_t* __restrict__ w, uint32_t i,
+                                           uint32_t check, uint32_t* err) {
+  fr_t acc = fr_zero();
+  for (uint32_t kx = rp[i], ke = rp[i + 1]; kx < ke; kx++) {
+    const fr_t wv = fr_ldg(w + col[kx]);
+    if (check) check_canonical(wv, err);
+    if (fr_is_zero(wv)) continue;
+    const fr_t cv = fr_ldg(val + kx);
+    acc = fr_add(acc, fr_is_mont_one(wv) ? cv : fr_mul(cv, wv));
+  }
+  return fr_canon(acc);
+}
+
+__device__ __forceinline__ fr_t gather_c(const fr_t& a, const fr_t& b) {
+  return (fr_is_zero(a) || fr_is_zero(b)) ? fr_zero() : fr_canon(fr_mul(a, b));
+}
+
+// Threads of a slice kernel: one per butterfly up to kSliceThreads.
+#ifndef G3H_SLICE_THREADS
+#define G3H_SLICE_THREADS 256
+#endif
+constexpr uint32_t kSliceThreads = G3H_SLICE_THREADS;
+#ifndef G3H_PASS_UNROLL
+#define G3H_PASS_UNROLL 1
+#endif
+constexpr int kPassUnroll = G3H_PASS_UNROLL;
+// Four resident blocks of 256 threads per SM (up to 64 registers each) measured best.
+#ifndef G3H_SLICE_MIN_BLOCKS
+#define G3H_SLICE_MIN_BLOCKS 4
+#endif
 
 // Butterfly of the pass on slice bit lb: index bf in [0, 2^(kk-1)) -> lower element lo,
 // upper element lo + 2^lb, and the twiddle table index of the element bit c0 + lb:
@@ -96,40 +150,55 @@ struct Bfly {
   uint32_t lo, hi, tw;
 };
 
-__device__ __forceinline__ Bfly bfly_at(uint32_t bf, uint32_t lb, uint32_t low, uint32_t c0,
-                                        uint32_t k) {
+// Butterfly order within a pass: for lb <= kk - 6 the index runs j-major (bf = j * Q + q,
+// Q = 2^(kk-1-lb) >= 32), so the 32 lanes of a warp share one twiddle index; above
+// that, q-major (bf = q * 2^lb + j). Both orders visit every butterfly once.
+__device__ __forceinline__ Bfly bfly_at(uint32_t bf, uint32_t lb, uint32_t kk, uint32_t low,
+                                        uint32_t c0, uint32_t k) {
   Bfly b;
-  const uint32_t j = bf & ((1u << lb) - 1u);
-  b.lo = ((bf >> lb) << (lb + 1u)) | j;
+  uint32_t j, q;
+  if (lb + 6u <= kk) {
+    j = bf >> (kk - 1u - lb);
+    q = bf & ((1u << (kk - 1u - lb)) - 1u);
+  } else {
+    j = bf & ((1u << lb) - 1u);
+    q = bf >> lb;
+  }
+  b.lo = (q << (lb + 1u)) | j;
   b.hi = b.lo + (1u << lb);
   b.tw = (low + (j << c0)) << (k - 1u - c0 - lb);
   return b;
 }
 
+// Twiddle index 0 is omega^0 = 1. In the warp-uniform (j-major) passes a whole warp
+// shares it, so the multiply is skipped without divergence; in pass 0 of element bit 0
+// every butterfly has it.
+
 // One decimation-in-frequency pass over the slice in shared memory, then a barrier.
-// When the pass is on element bit 0 every twiddle is 1 and the multiply is skipped.
-__device__ __forceinline__ void dif_pass(uint4* sm, uint32_t size, const fr_t* __restrict__ tw,
+__device__ __forceinline__ void dif_pass(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
                                          uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
-  const bool unit = (c0 + lb) == 0u;
+  const uint32_t size = 1u << kk;
+#pragma unroll kPassUnroll
   for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
-    const Bfly b = bfly_at(bf, lb, low, c0, k);
+    const Bfly b = bfly_at(bf, lb, kk, low, c0, k);
     const fr_t u = sm_get(sm, size, b.lo), v = sm_get(sm, size, b.hi);
     fr_t d = fr_sub(u, v);
     sm_put(sm, size, b.lo, fr_add(u, v));
-    if (!unit) d = fr_mul(d, fr_ldg(tw + b.tw));
+    if (b.tw != 0u) d = fr_mul_c(d, fr_const_ldg(tw + b.tw));
     sm_put(sm, size, b.hi, d);
   }
   __syncthreads();
 }
 
 // One decimation-in-time pass, then a barrier.
-__device__ __forceinline__ void dit_pass(uint4* sm, uint32_t size, const fr_t* __restrict__ tw,
+__device__ __forceinline__ void dit_pass(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
                                          uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
-  const bool unit = (c0 + lb) == 0u;
+  const uint32_t size = 1u << kk;
+#pragma unroll kPassUnroll
   for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
-    const Bfly b = bfly_at(bf, lb, low, c0, k);
+    const Bfly b = bfly_at(bf, lb, kk, low, c0, k);
     fr_t v = sm_get(sm, size, b.hi);
-    if (!unit) v = fr_mul(v, fr_ldg(tw + b.tw));
+    if (b.tw != 0u) v = fr_mul_c(v, fr_const_ldg(tw + b.tw));
     const fr_t u = sm_get(sm, size, b.lo);
     sm_put(sm, size, b.lo, fr_add(u, v));
     sm_put(sm, size, b.hi, fr_sub(u, v));
@@ -146,22 +215,31 @@ __device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t k
 // ---------------------------------------------------------------------------------------
 // k_ntt_dif: decimation-in-frequency passes over slice bits [c0, c0 + kk) of vector
 // blockIdx.y, src -> dst (in place when equal: every block reads its whole slice before
-// it writes). Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), dynamic shared
-// memory 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads) k_ntt_dif(const __grid_constant__ SliceArgs p) {
+// it writes). With SL_C_FROM_AB vector 2 is formed as a * b from vectors 0 and 1 at load.
+// Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), dynamic shared memory
+// 2^kk * 32 bytes.
+__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
   const size_t base = slice_base(blockIdx.x, c0, kk);
   const fr_t* src = p.src[blockIdx.y];
   fr_t* dst = p.dst[blockIdx.y];
-  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
-    const fr_t x = fr_load(src + base + ((size_t)m << c0));
-    if (p.mode & SL_CHECK) check_canonical(x, p.err);
-    sm_put(sm, size, m, x);
+  const uint32_t check = p.mode & SL_CHECK;
+  if ((p.mode & SL_C_FROM_AB) && blockIdx.y == 2u) {
+    for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+      const size_t i = base + ((size_t)m << c0);
+      sm_put(sm, size, m, gather_c(fr_load(p.src[0] + i), fr_load(p.src[1] + i)));
+    }
+  } else {
+    for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+      const fr_t x = fr_load(src + base + ((size_t)m << c0));
+      if (check) check_canonical(x, p.err);
+      sm_put(sm, size, m, x);
+    }
   }
   __syncthreads();
-  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, size, p.tw, (uint32_t)lb, low, c0, k);
+  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, kk, p.tw, (uint32_t)lb, low, c0, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(dst + base + ((size_t)m << c0), sm_get(sm, size, m));
 }
@@ -173,7 +251,7 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_dif(const __grid_constant
 // then the forward transform's decimation-in-time passes on bits 0 .. kk-1 (twiddles
 // p.tw2). In place. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
 // 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads) k_ntt_mid(const __grid_constant__ SliceArgs p) {
+__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_mid(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
@@ -181,11 +259,11 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_mid(const __grid_constant
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_load(vec + base + m));
   __syncthreads();
-  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, size, p.tw, (uint32_t)lb, 0u, 0u, k);
+  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, kk, p.tw, (uint32_t)lb, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
-    sm_put(sm, size, m, fr_mul(sm_get(sm, size, m), fr_ldg(p.scale_tab + base + m)));
+    sm_put(sm, size, m, fr_mul_c(sm_get(sm, size, m), fr_const_ldg(p.scale_tab + base + m)));
   __syncthreads();
-  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw2, lb, 0u, 0u, k);
+  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw2, lb, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(vec + base + m, sm_get(sm, size, m));
 }
@@ -198,9 +276,13 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_mid(const __grid_constant
 //   stored to dst[0], dst[1], and at c's store every thread re-reads the a and b values
 //   it stored itself and writes h = a*b - c to h_mont and from_mont(h) to h_std
 //   (the POINTWISE_CU join fused into the last transform's store).
-// Launch: grid (n >> kk, vectors or 1 with SL_JOIN), block min(2^(kk-1), 256), shared
+//   SL_JOIN_LAST: block (s, v) runs vector v of slice s and stores it to dst[v]; the
+//   three blocks of a slice then count themselves in on counters[s] (each thread fences
+//   its stores first), and the block that arrives third reads a, b, c of the slice from
+//   L2 and writes h, then resets the counter. No block ever waits for another.
+// Launch: grid (n >> kk, vectors; 1 with SL_JOIN), block min(2^(kk-1), 256), shared
 // 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads) k_ntt_dit(const __grid_constant__ SliceArgs p) {
+__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dit(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
@@ -215,7 +297,7 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_dit(const __grid_constant
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
       sm_put(sm, size, m, fr_load(src + base + ((size_t)m << c0)));
     __syncthreads();
-    for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw, lb, low, c0, k);
+    for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw, lb, low, c0, k);
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
       const size_t i = base + ((size_t)m << c0);
       const fr_t x = sm_get(sm, size, m);
@@ -225,14 +307,35 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_dit(const __grid_constant
         const fr_t h = fr_canon(fr_sub(fr_mul(a, b), x));
         fr_store(p.h_mont + i, h);
         fr_store(p.h_std + i, fr_from_mont(h));
-      } else if (join) {
+      } else if (join || (p.mode & SL_JOIN_LAST)) {
         fr_store(dst + i, x);
       } else {
         fr_t y = x;
-        if (p.mode & SL_SCALE_TABLE) y = fr_mul(y, fr_ldg(p.scale_tab + i));
-        if (p.mode & SL_SCALE_CONST) y = fr_mul(y, p.kscale);
+        if (p.mode & SL_SCALE_TABLE) y = fr_mul_c(y, fr_const_ldg(p.scale_tab + i));
+        if (p.mode & SL_SCALE_CONST) y = fr_mul_c(y, p.kscale);
         fr_store(dst + i, fr_canon(y));
       }
+    }
+  }
+  if (p.mode & SL_JOIN_LAST) {
+    __shared__ uint32_t arrived;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      arrived = atomicAdd(p.counters + blockIdx.x, 1u);
+      __threadfence();
+    }
+    __syncthreads();
+    if (arrived == 2u) {
+      for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
+        const size_t i = base + ((size_t)m << c0);
+        const fr_t a = fr_ldcg(p.dst[0] + i), b = fr_ldcg(p.dst[1] + i);
+        const fr_t c = fr_ldcg(p.dst[2] + i);
+        const fr_t h = fr_canon(fr_sub(fr_mul(a, b), c));
+        fr_store(p.h_mont + i, h);
+        fr_store(p.h_std + i, fr_from_mont(h));
+      }
+      if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
     }
   }
 }
@@ -244,7 +347,7 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_dit(const __grid_constant
 // page), scaled by scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and
 // the result goes to dst (out of place: a block reads other blocks' elements).
 // Launch: grid (n >> kk), block min(2^(kk-1), 256), shared 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads) k_ntt_brev(const __grid_constant__ SliceArgs p) {
+__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_brev(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
@@ -252,12 +355,12 @@ __global__ void __launch_bounds__(kSliceThreads) k_ntt_brev(const __grid_constan
     const uint32_t j = bitrev((uint32_t)base + m, k);
     fr_t x = fr_load(p.src[0] + j);
     if (p.mode & SL_CHECK) check_canonical(x, p.err);
-    if (p.mode & SL_SCALE_TABLE) x = fr_mul(x, fr_ldg(p.scale_tab + j));
-    if (p.mode & SL_SCALE_CONST) x = fr_mul(x, p.kscale);
+    if (p.mode & SL_SCALE_TABLE) x = fr_mul_c(x, fr_const_ldg(p.scale_tab + j));
+    if (p.mode & SL_SCALE_CONST) x = fr_mul_c(x, p.kscale);
     sm_put(sm, size, m, x);
   }
   __syncthreads();
-  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, size, p.tw, lb, 0u, 0u, k);
+  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw, lb, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(p.dst[0] + base + m, sm_get(sm, size, m));
 }
