@@ -133,7 +133,7 @@ int g3h_mul(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, uint32_t* out, s
  * no counterpart on the pages; it is this library's own addition.
  *
  * It needs no context and allocates nothing: its working vectors and domain tables live in
- * one fixed device array of 10 MiB inside the library, reserved on every GPU that loads
+ * one fixed device array of 14 MiB inside the library, reserved on every GPU that loads
  * the library until the process exits. Hence log_n <= 16 (domains up to 2^16 points);
  * larger domains return G3H_E_RANGE without doing anything.
  *
