@@ -84,6 +84,20 @@ Plan plan_for(uint32_t k) {
 
 }  // namespace
 
+// One set of per-computation buffers and the stream that uses them. Lane 0 is the
+// context's own stream and buffers; batched calls add lanes so that consecutive
+// computations overlap (one lane's gather and kernel tails run beside another's NTTs).
+struct Lane {
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  fr_t* abc = nullptr;        // 3n: a | b | c while they are transformed
+  fr_t* ab_in = nullptr;      // 2n: the gather's a | b
+  uint32_t* counters = nullptr;  // fused join: one per top-level slice, kept zero
+  fr_t* stage = nullptr;      // host-pointer calls: witness | h_mont | h_std
+  size_t stage_elems = 0;
+  cudaEvent_t done = nullptr;
+};
+
 struct g3h_ctx {
   int device = 0;
   cudaStream_t stream = nullptr;
@@ -106,6 +120,8 @@ struct g3h_ctx {
   size_t stage_elems = 0;
   uint32_t* d_err = nullptr;
   fr_const_t h_ninv;  // host copy of n^-1, passed by value to kernels
+  std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
+  cudaEvent_t batch_start = nullptr;
   bool timing = false;
   std::vector<TimedLaunch> launches;
   std::vector<cudaEvent_t> event_pool;
@@ -128,6 +144,14 @@ void release(g3h_ctx* c) {
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+  for (Lane& l : c->extra_lanes) {
+    void* lb[] = {l.abc, l.ab_in, l.counters, l.stage};
+    for (void* b : lb)
+      if (b) cudaFree(b);
+    if (l.done) cudaEventDestroy(l.done);
+    if (l.own_stream && l.stream) cudaStreamDestroy(l.stream);
+  }
+  if (c->batch_start) cudaEventDestroy(c->batch_start);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
 }
 
@@ -141,30 +165,40 @@ cudaEvent_t take_event(g3h_ctx* c) {
 }
 
 template <class F>
-int run(g3h_ctx* c, const char* name, F&& launch) {
+int run_on(g3h_ctx* c, cudaStream_t st, const char* name, F&& launch) {
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (c->timing) {
     e0 = take_event(c);
     e1 = take_event(c);
-    if (e0 && e1) cudaEventRecord(e0, c->stream);
+    if (e0 && e1) cudaEventRecord(e0, st);
   }
   launch();
   const cudaError_t err = cudaGetLastError();
   if (c->timing && e0 && e1) {
-    cudaEventRecord(e1, c->stream);
+    cudaEventRecord(e1, st);
     c->launches.push_back({name, e0, e1});
   }
   return err == cudaSuccess ? G3H_OK : G3H_E_CUDA;
 }
 
+template <class F>
+int run(g3h_ctx* c, const char* name, F&& launch) {
+  return run_on(c, c->stream, name, static_cast<F&&>(launch));
+}
+
 unsigned blocks_for(size_t count, unsigned per) { return (unsigned)((count + per - 1) / per); }
 
-int launch_slice(g3h_ctx* c, const char* name, void (*kern)(SliceArgs), const SliceArgs& a,
-                 unsigned nvec) {
+int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, void (*kern)(SliceArgs),
+                    const SliceArgs& a, unsigned nvec) {
   const dim3 grid((unsigned)(c->n >> a.kk), nvec);
   const dim3 block(std::min(1u << (a.kk - 1u), kSliceThreads));
   const size_t smem = (size_t)32 << a.kk;
-  return run(c, name, [&] { kern<<<grid, block, smem, c->stream>>>(a); });
+  return run_on(c, st, name, [&] { kern<<<grid, block, smem, st>>>(a); });
+}
+
+int launch_slice(g3h_ctx* c, const char* name, void (*kern)(SliceArgs), const SliceArgs& a,
+                 unsigned nvec) {
+  return launch_slice_on(c, c->stream, name, kern, a, nvec);
 }
 
 int set_smem_limits() {
@@ -205,18 +239,17 @@ int ensure_stage(g3h_ctx* c, size_t elems) {
   return G3H_OK;
 }
 
-int h2d(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
+int copy_on(cudaStream_t st, void* dst, const void* src, size_t bytes, cudaMemcpyKind kind) {
   if (bytes == 0) return G3H_OK;
-  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, c->stream) == cudaSuccess
-             ? G3H_OK
-             : G3H_E_CUDA;
+  return cudaMemcpyAsync(dst, src, bytes, kind, st) == cudaSuccess ? G3H_OK : G3H_E_CUDA;
+}
+
+int h2d(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
+  return copy_on(c->stream, dst, src, bytes, cudaMemcpyHostToDevice);
 }
 
 int d2h(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
-  if (bytes == 0) return G3H_OK;
-  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, c->stream) == cudaSuccess
-             ? G3H_OK
-             : G3H_E_CUDA;
+  return copy_on(c->stream, dst, src, bytes, cudaMemcpyDeviceToHost);
 }
 
 // Waits for the stream and reports (then clears) the device-side input check word.
@@ -241,29 +274,41 @@ SliceArgs base_args(g3h_ctx* c, uint32_t flags) {
   return a;
 }
 
-int gather(g3h_ctx* c, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc, uint32_t flags);
+int gather_on(g3h_ctx* c, cudaStream_t st, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc,
+              uint32_t flags);
 
-// Steps 2-5 on device vectors a, b, c -> h_mont, h_std (device). a, b, c may be the
-// context's scratch vectors. With a witness w (device) instead, steps 1-5: the gather
-// is fused into the load of the first inverse kernel (a, b, c are then ignored).
-int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_t* w, fr_t* hm,
-             fr_t* hs, uint32_t flags) {
+Lane lane0(g3h_ctx* c) {
+  Lane l;
+  l.stream = c->stream;
+  l.abc = c->d_abc;
+  l.ab_in = c->d_ab_in;
+  l.counters = c->d_counters;
+  return l;
+}
+
+// Steps 2-5 on device vectors a, b, c -> h_mont, h_std (device), on a lane's stream and
+// buffers. a, b, c may be the lane's scratch vectors. With a witness w (device) instead,
+// steps 1-5: the gather writes a and b and the first inverse kernel forms c = a * b at
+// its load (a, b, c are then ignored).
+int quotient(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b, const fr_t* cc,
+             const fr_t* w, fr_t* hm, fr_t* hs, uint32_t flags) {
   const uint32_t k = c->log_n;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   const size_t n = c->n;
+  const cudaStream_t st = ln.stream;
   if (w && k <= kSmallMaxLog) {
-    fr_t* s3 = c->d_abc;
-    const int rc = gather(c, w, s3, s3 + n, s3 + 2 * n, flags);
+    fr_t* s3 = ln.abc;
+    const int rc = gather_on(c, st, w, s3, s3 + n, s3 + 2 * n, flags);
     if (rc != G3H_OK) return rc;
     a = s3;
     b = s3 + n;
     cc = s3 + 2 * n;
   } else if (w) {
     // a and b by the gather; c = a * b is formed by the first inverse kernel at load
-    fr_t* ab = c->d_ab_in;
+    fr_t* ab = ln.ab_in;
     const uint32_t chk = check;
-    const int rc = run(c, "gather", [&] {
-      k_gather_ab<<<blocks_for(2 * n, 256), 256, 0, c->stream>>>(
+    const int rc = run_on(c, st, "gather", [&] {
+      k_gather_ab<<<blocks_for(2 * n, 256), 256, 0, st>>>(
           c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
           c->n_rows_b, (uint32_t)n, ab, ab + n, chk, c->d_err);
     });
@@ -273,12 +318,12 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_
     cc = nullptr;
   }
   if (k <= kSmallMaxLog) {
-    return run(c, "small_quotient", [&] {
-      k_small_quotient<<<1, 32, 0, c->stream>>>(a, b, cc, c->d_tw_inv, c->d_tw_fwd,
-                                                 c->d_shift_br, hm, hs, k, check, c->d_err);
+    return run_on(c, st, "small_quotient", [&] {
+      k_small_quotient<<<1, 32, 0, st>>>(a, b, cc, c->d_tw_inv, c->d_tw_fwd, c->d_shift_br, hm,
+                                          hs, k, check, c->d_err);
     });
   }
-  fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
+  fr_t* s[3] = {ln.abc, ln.abc + n, ln.abc + 2 * n};
   const Plan pl = plan_for(k);
   int rc = G3H_OK;
   // inverse, top levels first
@@ -294,7 +339,7 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_
     x.c0 = pl.c0[lvl];
     x.mode = (first && check && !w) ? SL_CHECK : 0u;
     if (first && w) x.mode |= SL_C_FROM_AB;
-    rc = launch_slice(c, "ntt_dif", k_ntt_dif, x, 3);
+    rc = launch_slice_on(c, st, "ntt_dif", k_ntt_dif, x, 3);
   }
   if (rc != G3H_OK) return rc;
   {
@@ -305,7 +350,7 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_
     x.scale_tab = c->d_shift_br;
     x.kk = pl.kk[0];
     x.c0 = 0;
-    rc = launch_slice(c, "ntt_mid", k_ntt_mid, x, 3);
+    rc = launch_slice_on(c, st, "ntt_mid", k_ntt_mid, x, 3);
   }
   // forward, middle levels
   for (int lvl = 1; lvl < pl.levels - 1 && rc == G3H_OK; lvl++) {
@@ -314,7 +359,7 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_
     x.tw = c->d_tw_fwd;
     x.kk = pl.kk[lvl];
     x.c0 = pl.c0[lvl];
-    rc = launch_slice(c, "ntt_dit", k_ntt_dit, x, 3);
+    rc = launch_slice_on(c, st, "ntt_dit", k_ntt_dit, x, 3);
   }
   if (rc != G3H_OK) return rc;
   const int top = pl.levels - 1;
@@ -323,28 +368,33 @@ int quotient(g3h_ctx* c, const fr_t* a, const fr_t* b, const fr_t* cc, const fr_
   x.tw = c->d_tw_fwd;
   x.kk = pl.kk[top];
   x.c0 = pl.c0[top];
-  if (!(flags & G3H_UNFUSED_JOIN)) {
+  if (flags & G3H_FUSED_JOIN) {
     x.mode = SL_JOIN_LAST;
     x.h_mont = hm;
     x.h_std = hs;
-    x.counters = c->d_counters;
-    return launch_slice(c, "ntt_dit_join", k_ntt_dit, x, 3);
+    x.counters = ln.counters;
+    return launch_slice_on(c, st, "ntt_dit_join", k_ntt_dit, x, 3);
   }
-  rc = launch_slice(c, "ntt_dit", k_ntt_dit, x, 3);
+  rc = launch_slice_on(c, st, "ntt_dit", k_ntt_dit, x, 3);
   if (rc != G3H_OK) return rc;
-  return run(c, "join", [&] {
-    k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
+  return run_on(c, st, "join", [&] {
+    k_join<<<blocks_for(n, 256), 256, 0, st>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
+  });
+}
+
+int gather_on(g3h_ctx* c, cudaStream_t st, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc,
+              uint32_t flags) {
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  const uint32_t n = (uint32_t)c->n;
+  return run_on(c, st, "gather", [&] {
+    k_gather<<<blocks_for(n, 256), 256, 0, st>>>(
+        c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
+        c->n_rows_b, n, a, b, cc, check, c->d_err);
   });
 }
 
 int gather(g3h_ctx* c, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc, uint32_t flags) {
-  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
-  const uint32_t n = (uint32_t)c->n;
-  return run(c, "gather", [&] {
-    k_gather<<<blocks_for(n, 256), 256, 0, c->stream>>>(
-        c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
-        c->n_rows_b, n, a, b, cc, check, c->d_err);
-  });
+  return gather_on(c, c->stream, w, a, b, cc, flags);
 }
 
 int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
@@ -533,15 +583,15 @@ int g3h_compute_h(g3h_ctx* c, const uint32_t* witness, uint32_t* h_mont, uint32_
   const size_t n = c->n;
   fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
   if (flags & G3H_DEVICE_PTRS)
-    return quotient(c, s[0], s[1], s[2], (const fr_t*)witness, (fr_t*)h_mont, (fr_t*)h_std,
-                    flags);
+    return quotient(c, lane0(c), s[0], s[1], s[2], (const fr_t*)witness, (fr_t*)h_mont,
+                    (fr_t*)h_std, flags);
   int rc = ensure_stage(c, (size_t)c->n_wires + 2 * n);
   if (rc != G3H_OK) return rc;
   fr_t* w = c->d_stage;
   fr_t* hm = c->d_stage + c->n_wires;
   fr_t* hs = hm + n;
   rc = h2d(c, w, witness, (size_t)c->n_wires * sizeof(fr_t));
-  if (rc == G3H_OK) rc = quotient(c, s[0], s[1], s[2], w, hm, hs, flags);
+  if (rc == G3H_OK) rc = quotient(c, lane0(c), s[0], s[1], s[2], w, hm, hs, flags);
   if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
   const int rc2 = finish(c);
@@ -554,8 +604,8 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
   DeviceGuard guard(c->device);
   const size_t n = c->n;
   if (flags & G3H_DEVICE_PTRS)
-    return quotient(c, (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, nullptr, (fr_t*)h_mont,
-                    (fr_t*)h_std, flags);
+    return quotient(c, lane0(c), (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, nullptr,
+                    (fr_t*)h_mont, (fr_t*)h_std, flags);
   int rc = ensure_stage(c, 5 * n);
   if (rc != G3H_OK) return rc;
   fr_t* in = c->d_stage;
@@ -564,9 +614,108 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
   rc = h2d(c, in, a, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = h2d(c, in + n, b, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = h2d(c, in + 2 * n, cc, n * sizeof(fr_t));
-  if (rc == G3H_OK) rc = quotient(c, in, in + n, in + 2 * n, nullptr, hm, hs, flags);
+  if (rc == G3H_OK) rc = quotient(c, lane0(c), in, in + n, in + 2 * n, nullptr, hm, hs, flags);
   if (rc == G3H_OK) rc = d2h(c, h_mont, hm, n * sizeof(fr_t));
   if (rc == G3H_OK) rc = d2h(c, h_std, hs, n * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Lanes of a batched call: the context's own plus up to kBatchLanes - 1 more, each with
+// its stream and buffers, allocated on first use and kept.
+constexpr uint32_t kBatchLanes = 3;
+
+int ensure_lanes(g3h_ctx* c, uint32_t lanes, bool staged) {
+  const size_t n = c->n;
+  const Plan pl = plan_for(c->log_n);
+  const size_t n_slices = std::max<size_t>(n >> pl.kk[pl.levels - 1], 1);
+  while (c->extra_lanes.size() + 1 < lanes) {
+    c->extra_lanes.emplace_back();
+    Lane& l = c->extra_lanes.back();
+    if (cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) != cudaSuccess)
+      return G3H_E_CUDA;
+    l.own_stream = true;
+    int rc = dalloc(&l.abc, 3 * n);
+    if (rc == G3H_OK) rc = dalloc(&l.ab_in, 2 * n);
+    if (rc == G3H_OK) rc = dalloc(&l.counters, n_slices);
+    if (rc != G3H_OK) return rc;
+    if (cudaMemsetAsync(l.counters, 0, n_slices * sizeof(uint32_t), l.stream) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess)
+      return G3H_E_CUDA;
+  }
+  if (!c->batch_start &&
+      cudaEventCreateWithFlags(&c->batch_start, cudaEventDisableTiming) != cudaSuccess)
+    return G3H_E_CUDA;
+  if (staged) {
+    const size_t elems = (size_t)c->n_wires + 2 * n;
+    int rc = ensure_stage(c, elems);
+    if (rc != G3H_OK) return rc;
+    for (uint32_t i = 0; i + 1 < lanes; i++) {
+      Lane& l = c->extra_lanes[i];
+      if (l.stage_elems < elems) {
+        if (l.stage) cudaFree(l.stage);
+        l.stage = nullptr;
+        l.stage_elems = 0;
+        if (dalloc(&l.stage, elems) != G3H_OK) return G3H_E_NOMEM;
+        l.stage_elems = elems;
+      }
+    }
+  }
+  return G3H_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int g3h_compute_h_batch(g3h_ctx* c, uint32_t count, const uint32_t* witnesses,
+                        uint32_t* h_mont, uint32_t* h_std, uint32_t flags) {
+  if (!c || !c->has_csr) return G3H_E_INVAL;
+  if (count == 0) return G3H_OK;
+  if (!h_mont || !h_std || (!witnesses && c->n_wires)) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  const bool dev = (flags & G3H_DEVICE_PTRS) != 0u;
+  const uint32_t lanes = std::min(count, kBatchLanes);
+  int rc = ensure_lanes(c, lanes, !dev);
+  if (rc != G3H_OK) return rc;
+  // the extra lanes start after everything already queued on the context's stream
+  if (cudaEventRecord(c->batch_start, c->stream) != cudaSuccess) return G3H_E_CUDA;
+  for (uint32_t i = 0; i + 1 < lanes; i++)
+    if (cudaStreamWaitEvent(c->extra_lanes[i].stream, c->batch_start, 0) != cudaSuccess)
+      return G3H_E_CUDA;
+  const size_t n = c->n, nw = c->n_wires;
+  for (uint32_t i = 0; i < count && rc == G3H_OK; i++) {
+    const uint32_t li = i % lanes;
+    Lane ln = li == 0 ? lane0(c) : c->extra_lanes[li - 1];
+    if (li == 0) ln.stage = c->d_stage;
+    const uint32_t* wi = witnesses + (size_t)i * 8 * nw;
+    uint32_t* hmi = h_mont + (size_t)i * 8 * n;
+    uint32_t* hsi = h_std + (size_t)i * 8 * n;
+    if (dev) {
+      rc = quotient(c, ln, nullptr, nullptr, nullptr, (const fr_t*)wi, (fr_t*)hmi, (fr_t*)hsi,
+                    flags);
+      continue;
+    }
+    fr_t* w = ln.stage;
+    fr_t* hm = ln.stage + nw;
+    fr_t* hs = hm + n;
+    rc = copy_on(ln.stream, w, wi, nw * sizeof(fr_t), cudaMemcpyHostToDevice);
+    if (rc == G3H_OK) rc = quotient(c, ln, nullptr, nullptr, nullptr, w, hm, hs, flags);
+    if (rc == G3H_OK) rc = copy_on(ln.stream, hmi, hm, n * sizeof(fr_t), cudaMemcpyDeviceToHost);
+    if (rc == G3H_OK) rc = copy_on(ln.stream, hsi, hs, n * sizeof(fr_t), cudaMemcpyDeviceToHost);
+  }
+  // the context's stream waits for the extra lanes: the batch ends in its order
+  for (uint32_t i = 0; i + 1 < lanes; i++) {
+    Lane& l = c->extra_lanes[i];
+    if (cudaEventRecord(l.done, l.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(c->stream, l.done, 0) != cudaSuccess)
+      return G3H_E_CUDA;
+  }
+  if (dev) return rc;
   const int rc2 = finish(c);
   return rc != G3H_OK ? rc : rc2;
 }

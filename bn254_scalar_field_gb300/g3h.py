@@ -25,14 +25,15 @@ G3H_E_CUDA = -5
 
 G3H_DEVICE_PTRS = 0x1
 G3H_NOCHECK = 0x2
-G3H_UNFUSED_JOIN = 0x4
+G3H_FUSED_JOIN = 0x4
 
 # cudaStreamLegacy: the runtime's handle for the legacy default stream.
 CUDA_STREAM_LEGACY = 0x1
 
 ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather", "g3h_ntt",
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
-                "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static")
+                "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
+                "g3h_compute_h_batch")
 
 
 class G3HError(RuntimeError):
@@ -81,6 +82,7 @@ def lib():
         L.g3h_timing_read.argtypes = [P, ctypes.POINTER(g3h_kernel_time), I,
                                       ctypes.POINTER(I)]
         L.g3h_compute_h_abc_static.argtypes = [U, P, P, P, P, P, P]
+        L.g3h_compute_h_batch.argtypes = [P, U, P, P, P, U]
         for name in ENTRY_POINTS:
             if name not in ("g3h_destroy", "g3h_strerror"):
                 getattr(L, name).restype = ctypes.c_int
@@ -174,6 +176,15 @@ def g3h_compute_h(ctx, witness, h_mont, h_std, flags=0):
     _check(lib().g3h_compute_h(ctx, bufs[0][0], bufs[1][0], bufs[2][0], f), "g3h_compute_h")
 
 
+def g3h_compute_h_batch(ctx, witnesses, h_mont, h_std, flags=0):
+    """witnesses: (count, n_wires, 8); h_mont, h_std: (count, n, 8)."""
+    count = witnesses.shape[0] if witnesses.ndim == 3 else 1
+    bufs = [_ptr(witnesses, None), _ptr(h_mont, None), _ptr(h_std, None)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_compute_h_batch(ctx, count, bufs[0][0], bufs[1][0], bufs[2][0], f),
+           "g3h_compute_h_batch")
+
+
 def g3h_compute_h_abc(ctx, a, b, c, h_mont, h_std, flags=0):
     bufs = [_ptr(x, None) for x in (a, b, c, h_mont, h_std)]
     f = _flags(bufs, flags)
@@ -263,6 +274,9 @@ class Context:
 
     def compute_h(self, witness, h_mont, h_std, flags=0):
         g3h_compute_h(self.handle, witness, h_mont, h_std, flags)
+
+    def compute_h_batch(self, witnesses, h_mont, h_std, flags=0):
+        g3h_compute_h_batch(self.handle, witnesses, h_mont, h_std, flags)
 
     def compute_h_abc(self, a, b, c, h_mont, h_std, flags=0):
         g3h_compute_h_abc(self.handle, a, b, c, h_mont, h_std, flags)

@@ -60,11 +60,14 @@ extern "C" {
 /* flags */
 #define G3H_DEVICE_PTRS 0x1u  /* data pointers of this call are device pointers */
 #define G3H_NOCHECK 0x2u      /* skip the canonical-input checks */
-#define G3H_UNFUSED_JOIN 0x4u /* compute_h / compute_h_abc: finish the three forward
-                                 transforms, then run the standalone join kernel, instead
-                                 of the join fused into the last transform's store
-                                 (POINTWISE_CU: the unfused kernel the fused path is
-                                 checked against) */
+#define G3H_FUSED_JOIN 0x4u   /* compute_h / compute_h_abc: write h from the last forward
+                                 kernel (the last of a slice's three blocks to finish
+                                 joins that slice) instead of finishing the three forward
+                                 transforms and running the standalone join kernel
+                                 (POINTWISE_CU, g16_h_join). The pages fuse to save a read
+                                 of a, b, c; on GB300 these kernels are bound by the
+                                 integer multiplier and the standalone join measured
+                                 faster, so it is the default. Same results. */
 
 #define G3H_MAX_LOG_N 27
 
@@ -104,6 +107,17 @@ int g3h_compute_h(g3h_ctx* ctx, const uint32_t* witness, uint32_t* h_mont, uint3
  * pages' stages after the gather, for callers that already hold a, b and c. */
 int g3h_compute_h_abc(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, const uint32_t* c,
                       uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
+
+/* Steps 1-5 for `count` witnesses over the same prepared matrices (SURVEY's first
+ * "next" item, batched H): witness i is the n_wires elements at witnesses + 8*n_wires*i,
+ * its outputs the n elements at h_mont + 8*n*i and h_std + 8*n*i. Consecutive witnesses
+ * run on up to three streams with their own buffers (allocated by the first batched call
+ * and kept by the context), so that one computation's gather and kernel tails overlap
+ * another's transforms and, with host pointers, its copies (use pinned host memory for
+ * the copies to overlap). The batch completes in the order of the context's stream.
+ * Results are those of count separate g3h_compute_h calls. count = 0 does nothing. */
+int g3h_compute_h_batch(g3h_ctx* ctx, uint32_t count, const uint32_t* witnesses,
+                        uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
 
 /* Step 1 alone: a, b, c (n elements each, Montgomery) from the witness. */
 int g3h_gather(g3h_ctx* ctx, const uint32_t* witness, uint32_t* a, uint32_t* b, uint32_t* c,

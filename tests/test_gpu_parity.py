@@ -152,10 +152,10 @@ def test_compute_h_proving_key_configs(log_n):
         ctx.compute_h(w, hm, hs)
         assert np.array_equal(hm, want_m)
         assert np.array_equal(hs, want_s)
-        # the unfused join path (POINTWISE_CU: the reference the fused path is checked
-        # against) gives the same bits
+        # the join fused into the last forward kernel (POINTWISE_CU: the fused path the
+        # standalone join kernel checks) gives the same bits
         hm2, hs2 = _zeros(n), _zeros(n)
-        ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_UNFUSED_JOIN)
+        ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_FUSED_JOIN)
         assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
         # device pointers, asynchronous on the context's stream, twice in a row
         torch = _torch()
@@ -167,6 +167,40 @@ def test_compute_h_proving_key_configs(log_n):
             ctx.sync()
             assert np.array_equal(_host(hmd), want_m)
             assert np.array_equal(_host(hsd), want_s)
+
+
+@pytest.mark.parametrize("log_n", [4, 12, 14])
+def test_compute_h_batch(log_n):
+    """Batched H (several witnesses, one prepared context): every witness's output equals
+    the oracle's, with more witnesses than lanes, in host and device memory."""
+    A, B, w0 = synth.problem(log_n, seed=600 + log_n)
+    n = 1 << log_n
+    nw = w0.shape[0]
+    count = 5
+    ws = np.stack([w0] + [synth.witness(synth.SplitMix64(700 + i), nw, 0.9)
+                          for i in range(count - 1)])
+    want = [oracle.compute_h(log_n, A, B, ws[i]) for i in range(count)]
+    with g3h.Context(log_n, nw, A, B) as ctx:
+        hm = np.zeros((count, n, 8), np.uint32)
+        hs = np.zeros((count, n, 8), np.uint32)
+        ctx.compute_h_batch(ws, hm, hs)
+        for i in range(count):
+            assert np.array_equal(hm[i], want[i][0]) and np.array_equal(hs[i], want[i][1]), i
+        torch = _torch()
+        wd = torch.from_numpy(ws.view(np.int32)).cuda()
+        hmd = torch.zeros((count, n, 8), dtype=torch.int32, device="cuda")
+        hsd = torch.zeros((count, n, 8), dtype=torch.int32, device="cuda")
+        ctx.compute_h_batch(wd, hmd, hsd)
+        ctx.sync()
+        for i in range(count):
+            assert np.array_equal(_host(hmd[i]), want[i][0]), i
+            assert np.array_equal(_host(hsd[i]), want[i][1]), i
+        # one witness, and an empty batch
+        h1m = np.zeros((1, n, 8), np.uint32)
+        h1s = np.zeros((1, n, 8), np.uint32)
+        ctx.compute_h_batch(ws[2:3], h1m, h1s)
+        assert np.array_equal(h1m[0], want[2][0]) and np.array_equal(h1s[0], want[2][1])
+        assert g3h.lib().g3h_compute_h_batch(ctx.handle, 0, None, None, None, 0) == g3h.G3H_OK
 
 
 def test_compute_h_abc_stress_2_22():
@@ -290,5 +324,5 @@ def test_timing_records_kernels():
         ctx.compute_h(w, hm, hs)
         t = ctx.timing_read()
         ctx.timing_enable(False)
-    assert set(t) == {"gather", "ntt_dif", "ntt_mid", "ntt_dit_join"}
+    assert set(t) == {"gather", "ntt_dif", "ntt_mid", "ntt_dit", "join"}
     assert all(v[0] == 1 and v[1] > 0 for v in t.values())
