@@ -52,6 +52,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="skip the 2^22 secondary lines")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    p.add_argument("--serialize", action="store_true",
+                   help="headline pass too with the three vectors in one launch per phase "
+                        "on one stream (for profiler captures of the kernels as the "
+                        "roofline pass times them)")
     args = p.parse_args()
     ref = args.impl == "reference"
     if args.steps is None:
@@ -272,7 +276,11 @@ def main():
         """K steps, each bracketed by CUDA events on the launching stream, L2 flushed
         between steps outside the events. With per_kernel the library also records an
         event pair around each of its launches (a few microseconds per launch, so the
-        step times of that pass are not used for the headline)."""
+        step times of that pass are not used for the headline), and runs the three
+        vectors as one launch per phase on one stream (G3H_SERIALIZE), so that each
+        kernel's events bracket that kernel alone; by default the vectors run on three
+        streams whose kernels overlap."""
+        flags = g3h.G3H_SERIALIZE if (per_kernel or args.serialize) else 0
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         if dist:
@@ -283,7 +291,7 @@ def main():
         t_start = time.monotonic()
         for i in range(args.steps):
             evs[i][0].record(stream)
-            ctx.compute_h(wd, hm, hs)
+            ctx.compute_h(wd, hm, hs, flags=flags)
             evs[i][1].record(stream)
             flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
@@ -304,8 +312,12 @@ def main():
     value, step_s = combine_ranks(local_s, args.steps, dist, dev)
     step_ms = step_s * 1e3
     # second pass of the same K steps: per-kernel device times for the roofline
-    _, kt, _, _ = timed_steps(True)
-    launches = sum(v[0] for v in kt.values())
+    serial_s, kt, _, _ = timed_steps(True)
+    # launches per headline step (three streams): counted on one step
+    ctx.timing_enable(True)
+    ctx.compute_h(wd, hm, hs)
+    launches = args.steps * sum(v[0] for v in ctx.timing_read().values())
+    ctx.timing_enable(False)
 
     # roofline of the dominant kernel: algorithmic IMAD-class ops per launch / mean time
     top = max(kt, key=lambda k: kt[k][1])
@@ -336,8 +348,11 @@ def main():
         "peak_source": "derived: %d SMs x %d 32-bit IMAD results/clk/SM x %.0f MHz; a "
                        "32x32->64 product counts two" % (SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
         "whole_step_frac": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / peak_tops,
-        "timing": "step times from a pass without per-kernel events; kernel times from a "
-                  "second pass of the same K steps with the library's per-launch events",
+        "timing": "step times from a pass without per-kernel events (vectors on three "
+                  "streams); kernel times from a second pass of the same K steps with the "
+                  "library's per-launch events and the three vectors in one launch per "
+                  "phase on one stream (G3H_SERIALIZE), so each kernel runs alone",
+        "serialized_ms_per_step": serial_s * 1e3 / args.steps,
         "kernels_ms_per_step_sum": kernel_ms_sum,
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in kt.items()},
     }

@@ -96,7 +96,29 @@ struct Lane {
   fr_t* stage = nullptr;      // host-pointer calls: witness | h_mont | h_std
   size_t stage_elems = 0;
   cudaEvent_t done = nullptr;
+  // vectors b and c run on two more streams; events order them against the lane's stream
+  cudaStream_t aux[2] = {nullptr, nullptr};
+  cudaEvent_t ev_fork = nullptr, ev_ga = nullptr, ev_gb = nullptr;
+  cudaEvent_t ev_end[2] = {nullptr, nullptr};
 };
+
+int make_lane_streams(Lane& l) {
+  for (int i = 0; i < 2; i++)
+    if (cudaStreamCreateWithFlags(&l.aux[i], cudaStreamNonBlocking) != cudaSuccess)
+      return G3H_E_CUDA;
+  cudaEvent_t* evs[] = {&l.ev_fork, &l.ev_ga, &l.ev_gb, &l.ev_end[0], &l.ev_end[1]};
+  for (cudaEvent_t* e : evs)
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return G3H_E_CUDA;
+  return G3H_OK;
+}
+
+void free_lane_streams(Lane& l) {
+  for (int i = 0; i < 2; i++)
+    if (l.aux[i]) cudaStreamDestroy(l.aux[i]);
+  cudaEvent_t evs[] = {l.ev_fork, l.ev_ga, l.ev_gb, l.ev_end[0], l.ev_end[1]};
+  for (cudaEvent_t e : evs)
+    if (e) cudaEventDestroy(e);
+}
 
 struct g3h_ctx {
   int device = 0;
@@ -120,6 +142,7 @@ struct g3h_ctx {
   size_t stage_elems = 0;
   uint32_t* d_err = nullptr;
   fr_const_t h_ninv;  // host copy of n^-1, passed by value to kernels
+  Lane own;  // the auxiliary streams and events of lane 0 (its buffers are the fields above)
   std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
   cudaEvent_t batch_start = nullptr;
   bool timing = false;
@@ -149,8 +172,10 @@ void release(g3h_ctx* c) {
     for (void* b : lb)
       if (b) cudaFree(b);
     if (l.done) cudaEventDestroy(l.done);
+    free_lane_streams(l);
     if (l.own_stream && l.stream) cudaStreamDestroy(l.stream);
   }
+  free_lane_streams(c->own);
   if (c->batch_start) cudaEventDestroy(c->batch_start);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
 }
@@ -278,7 +303,7 @@ int gather_on(g3h_ctx* c, cudaStream_t st, const fr_t* w, fr_t* a, fr_t* b, fr_t
               uint32_t flags);
 
 Lane lane0(g3h_ctx* c) {
-  Lane l;
+  Lane l = c->own;
   l.stream = c->stream;
   l.abc = c->d_abc;
   l.ab_in = c->d_ab_in;
@@ -296,87 +321,115 @@ int quotient(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b, const fr_
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   const size_t n = c->n;
   const cudaStream_t st = ln.stream;
-  if (w && k <= kSmallMaxLog) {
-    fr_t* s3 = ln.abc;
-    const int rc = gather_on(c, st, w, s3, s3 + n, s3 + 2 * n, flags);
-    if (rc != G3H_OK) return rc;
-    a = s3;
-    b = s3 + n;
-    cc = s3 + 2 * n;
-  } else if (w) {
-    // a and b by the gather; c = a * b is formed by the first inverse kernel at load
-    fr_t* ab = ln.ab_in;
-    const uint32_t chk = check;
-    const int rc = run_on(c, st, "gather", [&] {
-      k_gather_ab<<<blocks_for(2 * n, 256), 256, 0, st>>>(
-          c->d_rpa, c->d_cola, c->d_vala, c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_a,
-          c->n_rows_b, (uint32_t)n, ab, ab + n, chk, c->d_err);
-    });
-    if (rc != G3H_OK) return rc;
-    a = ab;
-    b = ab + n;
-    cc = nullptr;
-  }
   if (k <= kSmallMaxLog) {
+    if (w) {
+      fr_t* s3 = ln.abc;
+      const int rc = gather_on(c, st, w, s3, s3 + n, s3 + 2 * n, flags);
+      if (rc != G3H_OK) return rc;
+      a = s3;
+      b = s3 + n;
+      cc = s3 + 2 * n;
+    }
     return run_on(c, st, "small_quotient", [&] {
       k_small_quotient<<<1, 32, 0, st>>>(a, b, cc, c->d_tw_inv, c->d_tw_fwd, c->d_shift_br, hm,
                                           hs, k, check, c->d_err);
     });
   }
+  // The three vectors are independent until the join: vector v runs on vs[v], so one
+  // vector's gather latency and kernel tails overlap the others' transforms. With
+  // G3H_SERIALIZE everything runs on the lane's stream, one launch per phase covering
+  // the three vectors (grid rows 0, 1, 2), so each kernel runs alone.
+  const bool serial = (flags & G3H_SERIALIZE) != 0u;
+  const cudaStream_t vs[3] = {st, serial ? st : ln.aux[0], serial ? st : ln.aux[1]};
+  const uint32_t nv = serial ? 1u : 3u;    // launches per phase
+  const unsigned rows = serial ? 3u : 1u;  // vectors per launch
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(ln.ev_fork, st)) || !ok(cudaStreamWaitEvent(vs[1], ln.ev_fork, 0)) ||
+      !ok(cudaStreamWaitEvent(vs[2], ln.ev_fork, 0)))
+    return G3H_E_CUDA;
+  int rc = G3H_OK;
+  if (w) {
+    // a and b by the gather, A on the stream of a, B on the stream of b; c = a * b is
+    // formed by c's first inverse kernel at its load, once both are done
+    fr_t* ab = ln.ab_in;
+    const uint32_t nn = (uint32_t)n;
+    rc = run_on(c, vs[0], "gather", [&] {
+      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(c->d_rpa, c->d_cola, c->d_vala, w,
+                                                            c->n_rows_a, nn, ab, check, c->d_err);
+    });
+    if (rc == G3H_OK)
+      rc = run_on(c, vs[1], "gather", [&] {
+        k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
+            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, ab + n, check, c->d_err);
+      });
+    if (rc != G3H_OK) return rc;
+    if (!ok(cudaEventRecord(ln.ev_ga, vs[0])) || !ok(cudaEventRecord(ln.ev_gb, vs[1])) ||
+        !ok(cudaStreamWaitEvent(vs[2], ln.ev_ga, 0)) || !ok(cudaStreamWaitEvent(vs[2], ln.ev_gb, 0)))
+      return G3H_E_CUDA;
+    a = ab;
+    b = ab + n;
+    cc = nullptr;
+  }
   fr_t* s[3] = {ln.abc, ln.abc + n, ln.abc + 2 * n};
   const Plan pl = plan_for(k);
-  int rc = G3H_OK;
+  // Launches are issued phase by phase over the three vectors so that the vectors
+  // advance together.
   // inverse, top levels first
   for (int lvl = pl.levels - 1; lvl >= 1 && rc == G3H_OK; lvl--) {
-    SliceArgs x = base_args(c, flags);
     const bool first = lvl == pl.levels - 1;
-    x.src[0] = first ? a : s[0];
-    x.src[1] = first ? b : s[1];
-    x.src[2] = first ? cc : s[2];
-    for (int v = 0; v < 3; v++) x.dst[v] = s[v];
-    x.tw = c->d_tw_inv;
-    x.kk = pl.kk[lvl];
-    x.c0 = pl.c0[lvl];
-    x.mode = (first && check && !w) ? SL_CHECK : 0u;
-    if (first && w) x.mode |= SL_C_FROM_AB;
-    rc = launch_slice_on(c, st, "ntt_dif", k_ntt_dif, x, 3);
+    for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
+      SliceArgs x = base_args(c, flags);
+      x.src[0] = first ? a : s[0];
+      x.src[1] = first ? b : s[1];
+      x.src[2] = first ? cc : s[2];
+      for (int u = 0; u < 3; u++) x.dst[u] = s[u];
+      x.tw = c->d_tw_inv;
+      x.kk = pl.kk[lvl];
+      x.c0 = pl.c0[lvl];
+      x.mode = (first && check && !w) ? SL_CHECK : 0u;
+      if (first && w) x.mode |= SL_C_FROM_AB;
+      x.vbase = v;
+      rc = launch_slice_on(c, vs[v], "ntt_dif", k_ntt_dif, x, rows);
+    }
   }
-  if (rc != G3H_OK) return rc;
-  {
+  for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
     SliceArgs x = base_args(c, flags);
-    for (int v = 0; v < 3; v++) x.dst[v] = s[v];
+    for (int u = 0; u < 3; u++) x.dst[u] = s[u];
     x.tw = c->d_tw_inv;
     x.tw2 = c->d_tw_fwd;
     x.scale_tab = c->d_shift_br;
     x.kk = pl.kk[0];
     x.c0 = 0;
-    rc = launch_slice_on(c, st, "ntt_mid", k_ntt_mid, x, 3);
+    x.vbase = v;
+    rc = launch_slice_on(c, vs[v], "ntt_mid", k_ntt_mid, x, rows);
   }
-  // forward, middle levels
-  for (int lvl = 1; lvl < pl.levels - 1 && rc == G3H_OK; lvl++) {
-    SliceArgs x = base_args(c, flags);
-    for (int v = 0; v < 3; v++) x.src[v] = x.dst[v] = s[v];
-    x.tw = c->d_tw_fwd;
-    x.kk = pl.kk[lvl];
-    x.c0 = pl.c0[lvl];
-    rc = launch_slice_on(c, st, "ntt_dit", k_ntt_dit, x, 3);
+  // forward, middle levels, then the top level
+  for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
+    const bool top = lvl == pl.levels - 1;
+    for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
+      SliceArgs x = base_args(c, flags);
+      for (int u = 0; u < 3; u++) x.src[u] = x.dst[u] = s[u];
+      x.tw = c->d_tw_fwd;
+      x.kk = pl.kk[lvl];
+      x.c0 = pl.c0[lvl];
+      x.vbase = v;
+      const bool fused = top && (flags & G3H_FUSED_JOIN);
+      if (fused) {
+        x.mode = SL_JOIN_LAST;
+        x.h_mont = hm;
+        x.h_std = hs;
+        x.counters = ln.counters;
+      }
+      rc = launch_slice_on(c, vs[v], fused ? "ntt_dit_join" : "ntt_dit", k_ntt_dit, x, rows);
+    }
   }
   if (rc != G3H_OK) return rc;
-  const int top = pl.levels - 1;
-  SliceArgs x = base_args(c, flags);
-  for (int v = 0; v < 3; v++) x.src[v] = x.dst[v] = s[v];
-  x.tw = c->d_tw_fwd;
-  x.kk = pl.kk[top];
-  x.c0 = pl.c0[top];
-  if (flags & G3H_FUSED_JOIN) {
-    x.mode = SL_JOIN_LAST;
-    x.h_mont = hm;
-    x.h_std = hs;
-    x.counters = ln.counters;
-    return launch_slice_on(c, st, "ntt_dit_join", k_ntt_dit, x, 3);
-  }
-  rc = launch_slice_on(c, st, "ntt_dit", k_ntt_dit, x, 3);
-  if (rc != G3H_OK) return rc;
+  // join: the lane's stream waits for vectors b and c
+  for (int i = 0; i < 2; i++)
+    if (!ok(cudaEventRecord(ln.ev_end[i], vs[i + 1])) ||
+        !ok(cudaStreamWaitEvent(st, ln.ev_end[i], 0)))
+      return G3H_E_CUDA;
+  if (flags & G3H_FUSED_JOIN) return G3H_OK;
   return run_on(c, st, "join", [&] {
     k_join<<<blocks_for(n, 256), 256, 0, st>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
   });
@@ -529,6 +582,7 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
     c->own_stream = true;
   }
   rc = set_smem_limits();
+  if (rc == G3H_OK) rc = make_lane_streams(c->own);
   if (rc == G3H_OK) rc = dalloc(&c->d_err, 1);
   if (rc == G3H_OK)
     rc = cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->stream) == cudaSuccess ? G3H_OK
@@ -646,6 +700,8 @@ int ensure_lanes(g3h_ctx* c, uint32_t lanes, bool staged) {
     if (cudaMemsetAsync(l.counters, 0, n_slices * sizeof(uint32_t), l.stream) != cudaSuccess ||
         cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess)
       return G3H_E_CUDA;
+    rc = make_lane_streams(l);
+    if (rc != G3H_OK) return rc;
   }
   if (!c->batch_start &&
       cudaEventCreateWithFlags(&c->batch_start, cudaEventDisableTiming) != cudaSuccess)

@@ -6,9 +6,10 @@
 namespace g3h {
 
 // ---------------------------------------------------------------------------------------
-// Step 1, the sums only: thread t < n forms a_t from row t of A, thread n + t forms b_t
-// from row t of B; c = a * b is then formed by the first inverse kernel at load
-// (SL_C_FROM_AB). Outputs canonical. Launch: ceil(2n / 256) blocks of 256.
+// Step 1, the sums of one matrix: thread i forms row i of A (or of B) against the
+// witness; the two matrices are launched separately, on separate streams, and c = a * b
+// is formed by the first inverse kernel of c at its load (SL_C_FROM_AB). Outputs
+// canonical. Launch: ceil(n / 256) blocks of 256.
 //
 // The kernel lasts as long as its slowest warp, and a row is a chain of dependent loads
 // (column, witness value, coefficient) per term, so the longest row (95 terms in the
@@ -36,27 +37,17 @@ __device__ __forceinline__ fr_t fr_shfl_xor(const fr_t& x, int lane_mask) {
   return y;
 }
 
-__global__ void __launch_bounds__(256) k_gather_ab(const uint32_t* __restrict__ rpa,
-                                                   const uint32_t* __restrict__ cola,
-                                                   const fr_t* __restrict__ vala,
-                                                   const uint32_t* __restrict__ rpb,
-                                                   const uint32_t* __restrict__ colb,
-                                                   const fr_t* __restrict__ valb,
-                                                   const fr_t* __restrict__ w,
-                                                   uint32_t n_rows_a, uint32_t n_rows_b,
-                                                   uint32_t n, fr_t* a_out, fr_t* b_out,
-                                                   uint32_t check, uint32_t* err) {
+__global__ void __launch_bounds__(256) k_gather_rows(const uint32_t* __restrict__ rp,
+                                                     const uint32_t* __restrict__ col,
+                                                     const fr_t* __restrict__ val,
+                                                     const fr_t* __restrict__ w,
+                                                     uint32_t n_rows, uint32_t n, fr_t* out,
+                                                     uint32_t check, uint32_t* err) {
   // No early return: every lane takes part in the warp-wide loop below.
-  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
-  const bool is_b = t >= n;
-  const uint32_t i = is_b ? t - n : t;
-  const bool valid = t < 2u * n && i < (is_b ? n_rows_b : n_rows_a);
-  const uint32_t* rp = is_b ? rpb : rpa;
-  const uint32_t* col = is_b ? colb : cola;
-  const fr_t* val = is_b ? valb : vala;
   uint32_t kx = 0, ke = 0;
-  if (valid) {
+  if (i < n && i < n_rows) {
     kx = rp[i];
     ke = rp[i + 1];
   }
@@ -70,25 +61,21 @@ __global__ void __launch_bounds__(256) k_gather_ab(const uint32_t* __restrict__ 
     }
     if (kx < ke) acc = fr_add(acc, gather_term(col, val, w, kx, check, err));
   }
-  // The warp's long rows, one at a time. The matrix is the same across a warp except at
-  // the A/B seam, so each long row carries its own matrix pointers through the shuffle.
+  // The warp's long rows, one at a time.
   uint32_t longs = __ballot_sync(0xffffffffu, !lane_row);
   while (longs) {
     const int src = __ffs(longs) - 1;
     longs &= longs - 1u;
     const uint32_t rb = __shfl_sync(0xffffffffu, kx, src);
     const uint32_t re = __shfl_sync(0xffffffffu, ke, src);
-    const bool rb_is_b = __shfl_sync(0xffffffffu, (uint32_t)is_b, src) != 0u;
-    const uint32_t* rcol = rb_is_b ? colb : cola;
-    const fr_t* rval = rb_is_b ? valb : vala;
     fr_t part = fr_zero();
     for (uint32_t k = rb + lane; k < re; k += 32u)
-      part = fr_add(part, gather_term(rcol, rval, w, k, check, err));
+      part = fr_add(part, gather_term(col, val, w, k, check, err));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part = fr_add(part, fr_shfl_xor(part, off));
     if ((int)lane == src) acc = part;
   }
-  if (t < 2u * n) fr_store((is_b ? b_out : a_out) + i, fr_canon(acc));
+  if (i < n) fr_store(out + i, fr_canon(acc));
 }
 
 // Step 1 alone (GATHER_CU, g16_gather_abc; gather_row in ntt.cuh). Outputs are canonical.

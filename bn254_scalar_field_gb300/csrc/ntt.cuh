@@ -66,6 +66,7 @@ struct SliceArgs {
   uint32_t c0;     // the slice's bits are [c0, c0 + kk) of the element index
   uint32_t mode;   // SL_* flags
   uint32_t* counters;  // SL_JOIN_LAST: one zeroed counter per slice, left zeroed
+  uint32_t vbase;      // vector of grid row blockIdx.y is vbase + blockIdx.y
 };
 
 // 16-byte slot of element m's half: the low three bits (the bank group of a 16-byte
@@ -214,7 +215,7 @@ __device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t k
 
 // ---------------------------------------------------------------------------------------
 // k_ntt_dif: decimation-in-frequency passes over slice bits [c0, c0 + kk) of vector
-// blockIdx.y, src -> dst (in place when equal: every block reads its whole slice before
+// vbase + blockIdx.y, src -> dst (in place when equal: every block reads its whole slice before
 // it writes). With SL_C_FROM_AB vector 2 is formed as a * b from vectors 0 and 1 at load.
 // Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), dynamic shared memory
 // 2^kk * 32 bytes.
@@ -223,10 +224,11 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
   const size_t base = slice_base(blockIdx.x, c0, kk);
-  const fr_t* src = p.src[blockIdx.y];
-  fr_t* dst = p.dst[blockIdx.y];
+  const uint32_t vec = p.vbase + blockIdx.y;
+  const fr_t* src = p.src[vec];
+  fr_t* dst = p.dst[vec];
   const uint32_t check = p.mode & SL_CHECK;
-  if ((p.mode & SL_C_FROM_AB) && blockIdx.y == 2u) {
+  if ((p.mode & SL_C_FROM_AB) && vec == 2u) {
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
       const size_t i = base + ((size_t)m << c0);
       sm_put(sm, size, m, gather_c(fr_load(p.src[0] + i), fr_load(p.src[1] + i)));
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif
 
 // ---------------------------------------------------------------------------------------
 // k_ntt_mid: on the contiguous slice of 2^kk elements starting at blockIdx.x << kk of
-// vector blockIdx.y: the inverse transform's decimation-in-frequency passes on bits
+// vector vbase + blockIdx.y: the inverse transform's decimation-in-frequency passes on bits
 // kk-1 .. 0 (twiddles p.tw), the shift by scale_tab[position] (g^brev(position) / n),
 // then the forward transform's decimation-in-time passes on bits 0 .. kk-1 (twiddles
 // p.tw2). In place. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_mid
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
-  fr_t* vec = p.dst[blockIdx.y];
+  fr_t* vec = p.dst[p.vbase + blockIdx.y];
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_load(vec + base + m));
   __syncthreads();
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dit
   const bool join = (p.mode & SL_JOIN) != 0u;
   const uint32_t nvec = join ? 3u : 1u;
   for (uint32_t vi = 0; vi < nvec; vi++) {
-    const uint32_t v = join ? vi : blockIdx.y;
+    const uint32_t v = join ? vi : p.vbase + blockIdx.y;
     const fr_t* src = p.src[v];
     fr_t* dst = p.dst[v];
     if (vi > 0) __syncthreads();  // the previous vector's last shared-memory reads

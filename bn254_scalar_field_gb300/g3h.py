@@ -26,6 +26,7 @@ G3H_E_CUDA = -5
 G3H_DEVICE_PTRS = 0x1
 G3H_NOCHECK = 0x2
 G3H_FUSED_JOIN = 0x4
+G3H_SERIALIZE = 0x8
 
 # cudaStreamLegacy: the runtime's handle for the legacy default stream.
 CUDA_STREAM_LEGACY = 0x1

@@ -69,6 +69,11 @@ extern "C" {
                                  integer multiplier and the standalone join measured
                                  faster, so it is the default. Same results. */
 
+#define G3H_SERIALIZE 0x8u    /* compute_h / compute_h_abc: run the three vectors' transforms
+                                 as one launch per phase on the context's stream instead
+                                 of one stream per vector, so that every kernel runs alone
+                                 (for per-kernel measurement). Same results. */
+
 #define G3H_MAX_LOG_N 27
 
 typedef struct g3h_ctx g3h_ctx;

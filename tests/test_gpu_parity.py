@@ -157,6 +157,11 @@ def test_compute_h_proving_key_configs(log_n):
         hm2, hs2 = _zeros(n), _zeros(n)
         ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_FUSED_JOIN)
         assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
+        # all on one stream, and fused on one stream
+        for fl in (g3h.G3H_SERIALIZE, g3h.G3H_SERIALIZE | g3h.G3H_FUSED_JOIN):
+            hm2, hs2 = _zeros(n), _zeros(n)
+            ctx.compute_h(w, hm2, hs2, flags=fl)
+            assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs), fl
         # device pointers, asynchronous on the context's stream, twice in a row
         torch = _torch()
         wd = _dev(w)
@@ -324,5 +329,15 @@ def test_timing_records_kernels():
         ctx.compute_h(w, hm, hs)
         t = ctx.timing_read()
         ctx.timing_enable(False)
-    assert set(t) == {"gather", "ntt_dif", "ntt_mid", "ntt_dit", "join"}
-    assert all(v[0] == 1 and v[1] > 0 for v in t.values())
+    # one stream per vector: two gathers (A, B), three launches per transform phase
+    assert {k: v[0] for k, v in t.items()} == {"gather": 2, "ntt_dif": 3, "ntt_mid": 3,
+                                               "ntt_dit": 3, "join": 1}
+    assert all(v[1] > 0 for v in t.values())
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        ctx.timing_enable(True)
+        hm2, hs2 = _zeros(n), _zeros(n)
+        ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_SERIALIZE)
+        t = ctx.timing_read()
+    assert {k: v[0] for k, v in t.items()} == {"gather": 2, "ntt_dif": 1, "ntt_mid": 1,
+                                               "ntt_dit": 1, "join": 1}
+    assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
