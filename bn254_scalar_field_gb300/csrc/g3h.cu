@@ -98,6 +98,8 @@ struct Lane {
   cudaEvent_t done = nullptr;
   // vectors b and c run on two more streams; events order them against the lane's stream
   cudaStream_t aux[2] = {nullptr, nullptr};
+  cudaStream_t cap = nullptr;  // launch graphs are captured here (the caller's stream may
+                               // be the legacy default stream, which cannot be captured)
   cudaEvent_t ev_fork = nullptr, ev_ga = nullptr, ev_gb = nullptr;
   cudaEvent_t ev_end[2] = {nullptr, nullptr};
 };
@@ -106,6 +108,7 @@ int make_lane_streams(Lane& l) {
   for (int i = 0; i < 2; i++)
     if (cudaStreamCreateWithFlags(&l.aux[i], cudaStreamNonBlocking) != cudaSuccess)
       return G3H_E_CUDA;
+  if (cudaStreamCreateWithFlags(&l.cap, cudaStreamNonBlocking) != cudaSuccess) return G3H_E_CUDA;
   cudaEvent_t* evs[] = {&l.ev_fork, &l.ev_ga, &l.ev_gb, &l.ev_end[0], &l.ev_end[1]};
   for (cudaEvent_t* e : evs)
     if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return G3H_E_CUDA;
@@ -115,6 +118,7 @@ int make_lane_streams(Lane& l) {
 void free_lane_streams(Lane& l) {
   for (int i = 0; i < 2; i++)
     if (l.aux[i]) cudaStreamDestroy(l.aux[i]);
+  if (l.cap) cudaStreamDestroy(l.cap);
   cudaEvent_t evs[] = {l.ev_fork, l.ev_ga, l.ev_gb, l.ev_end[0], l.ev_end[1]};
   for (cudaEvent_t e : evs)
     if (e) cudaEventDestroy(e);
@@ -143,6 +147,16 @@ struct g3h_ctx {
   uint32_t* d_err = nullptr;
   fr_const_t h_ninv;  // host copy of n^-1, passed by value to kernels
   Lane own;  // the auxiliary streams and events of lane 0 (its buffers are the fields above)
+  uint32_t* h_err = nullptr;  // pinned host copy of the device error word
+  // Launch graphs of quotient(): the per-H launches of one lane with one set of pointers
+  // and flags, captured once and replayed (fewer host calls per H, one graph launch).
+  struct Graph {
+    cudaStream_t stream;
+    const void* ptr[6];
+    uint32_t flags;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Graph> graphs;
   std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
   cudaEvent_t batch_start = nullptr;
   bool timing = false;
@@ -177,6 +191,8 @@ void release(g3h_ctx* c) {
   }
   free_lane_streams(c->own);
   if (c->batch_start) cudaEventDestroy(c->batch_start);
+  for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
+  if (c->h_err) cudaFreeHost(c->h_err);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
 }
 
@@ -279,12 +295,15 @@ int d2h(g3h_ctx* c, void* dst, const void* src, size_t bytes) {
 
 // Waits for the stream and reports (then clears) the device-side input check word.
 int finish(g3h_ctx* c) {
-  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
-  uint32_t err = 0;
-  if (cudaMemcpy(&err, c->d_err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+  // the error word comes back in the same stream, so one synchronisation covers both
+  if (cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                      c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess)
     return G3H_E_CUDA;
-  if (err) {
-    if (cudaMemset(c->d_err, 0, sizeof(uint32_t)) != cudaSuccess) return G3H_E_CUDA;
+  if (*c->h_err) {
+    *c->h_err = 0;
+    if (cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->stream) != cudaSuccess)
+      return G3H_E_CUDA;
     return G3H_E_NONCANON;
   }
   return G3H_OK;
@@ -315,8 +334,8 @@ Lane lane0(g3h_ctx* c) {
 // buffers. a, b, c may be the lane's scratch vectors. With a witness w (device) instead,
 // steps 1-5: the gather writes a and b and the first inverse kernel forms c = a * b at
 // its load (a, b, c are then ignored).
-int quotient(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b, const fr_t* cc,
-             const fr_t* w, fr_t* hm, fr_t* hs, uint32_t flags) {
+int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
+                      const fr_t* cc, const fr_t* w, fr_t* hm, fr_t* hs, uint32_t flags) {
   const uint32_t k = c->log_n;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   const size_t n = c->n;
@@ -433,6 +452,55 @@ int quotient(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b, const fr_
   return run_on(c, st, "join", [&] {
     k_join<<<blocks_for(n, 256), 256, 0, st>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
   });
+}
+
+// quotient_launches through a launch graph: captured on the first call with a given lane,
+// pointers and flags, replayed afterwards. Not when per-kernel timing is on (its events
+// must be recorded per call), when the caller's stream is already being captured, or
+// with G3H_NO_GRAPH.
+constexpr size_t kMaxGraphs = 8;
+
+int quotient(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b, const fr_t* cc,
+             const fr_t* w, fr_t* hm, fr_t* hs, uint32_t flags) {
+  const cudaStream_t st = ln.stream;
+  bool graph = !c->timing && !(flags & G3H_NO_GRAPH) && c->log_n > kSmallMaxLog;
+  if (graph) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return G3H_E_CUDA;
+    graph = cs == cudaStreamCaptureStatusNone;
+  }
+  if (!graph) return quotient_launches(c, ln, a, b, cc, w, hm, hs, flags);
+  const void* key[6] = {a, b, cc, w, hm, hs};
+  for (auto& g : c->graphs) {
+    if (g.stream == st && g.flags == flags && std::memcmp(g.ptr, key, sizeof(key)) == 0)
+      return cudaGraphLaunch(g.exec, st) == cudaSuccess ? G3H_OK : G3H_E_CUDA;
+  }
+  Lane cl = ln;  // the same buffers and streams, vector a captured on the private stream
+  cl.stream = ln.cap;
+  if (cudaStreamBeginCapture(cl.stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return G3H_E_CUDA;
+  int rc = quotient_launches(c, cl, a, b, cc, w, hm, hs, flags);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cl.stream, &g);
+  if (rc == G3H_OK && ec != cudaSuccess) rc = G3H_E_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (rc == G3H_OK && cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) rc = G3H_E_CUDA;
+  if (g) cudaGraphDestroy(g);
+  if (rc != G3H_OK) {
+    cudaGetLastError();
+    return rc;
+  }
+  if (c->graphs.size() == kMaxGraphs) {
+    cudaGraphExecDestroy(c->graphs.front().exec);
+    c->graphs.erase(c->graphs.begin());
+  }
+  g3h_ctx::Graph e;
+  e.stream = st;
+  std::memcpy(e.ptr, key, sizeof(key));
+  e.flags = flags;
+  e.exec = exec;
+  c->graphs.push_back(e);
+  return cudaGraphLaunch(exec, st) == cudaSuccess ? G3H_OK : G3H_E_CUDA;
 }
 
 int gather_on(g3h_ctx* c, cudaStream_t st, const fr_t* w, fr_t* a, fr_t* b, fr_t* cc,
@@ -583,6 +651,9 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
   }
   rc = set_smem_limits();
   if (rc == G3H_OK) rc = make_lane_streams(c->own);
+  if (rc == G3H_OK)
+    rc = cudaMallocHost((void**)&c->h_err, sizeof(uint32_t)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+  if (rc == G3H_OK) *c->h_err = 0;
   if (rc == G3H_OK) rc = dalloc(&c->d_err, 1);
   if (rc == G3H_OK)
     rc = cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->stream) == cudaSuccess ? G3H_OK
@@ -752,8 +823,9 @@ int g3h_compute_h_batch(g3h_ctx* c, uint32_t count, const uint32_t* witnesses,
     uint32_t* hmi = h_mont + (size_t)i * 8 * n;
     uint32_t* hsi = h_std + (size_t)i * 8 * n;
     if (dev) {
+      // every witness has its own buffers here: launch directly rather than capture
       rc = quotient(c, ln, nullptr, nullptr, nullptr, (const fr_t*)wi, (fr_t*)hmi, (fr_t*)hsi,
-                    flags);
+                    flags | G3H_NO_GRAPH);
       continue;
     }
     fr_t* w = ln.stage;

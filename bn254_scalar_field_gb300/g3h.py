@@ -27,6 +27,7 @@ G3H_DEVICE_PTRS = 0x1
 G3H_NOCHECK = 0x2
 G3H_FUSED_JOIN = 0x4
 G3H_SERIALIZE = 0x8
+G3H_NO_GRAPH = 0x10
 
 # cudaStreamLegacy: the runtime's handle for the legacy default stream.
 CUDA_STREAM_LEGACY = 0x1

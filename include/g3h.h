@@ -74,6 +74,10 @@ extern "C" {
                                  of one stream per vector, so that every kernel runs alone
                                  (for per-kernel measurement). Same results. */
 
+#define G3H_NO_GRAPH 0x10u    /* compute_h / compute_h_abc / compute_h_batch: issue the
+                                 launches one by one instead of replaying the context's
+                                 launch graph for these buffers and flags. Same results. */
+
 #define G3H_MAX_LOG_N 27
 
 typedef struct g3h_ctx g3h_ctx;

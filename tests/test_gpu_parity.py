@@ -157,8 +157,9 @@ def test_compute_h_proving_key_configs(log_n):
         hm2, hs2 = _zeros(n), _zeros(n)
         ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_FUSED_JOIN)
         assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
-        # all on one stream, and fused on one stream
-        for fl in (g3h.G3H_SERIALIZE, g3h.G3H_SERIALIZE | g3h.G3H_FUSED_JOIN):
+        # all on one stream, fused on one stream, and without the launch graph
+        for fl in (g3h.G3H_SERIALIZE, g3h.G3H_SERIALIZE | g3h.G3H_FUSED_JOIN,
+                   g3h.G3H_NO_GRAPH, g3h.G3H_NO_GRAPH | g3h.G3H_SERIALIZE):
             hm2, hs2 = _zeros(n), _zeros(n)
             ctx.compute_h(w, hm2, hs2, flags=fl)
             assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs), fl
