@@ -378,6 +378,7 @@ def main():
     extra = {"ntt_gelem_s_2^18_in_h": 6 * n / (step_ms / args.steps * 1e-3) / 1e9}
     extra.update(batched(torch, dev, ctx, w, n, flush))
     if not args.no_extra and rank == 0:
+        extra.update(other_domains(torch, dev, g3h, synth, flush))
         extra.update(stress_2_22(torch, dev, g3h, synth))
     ctx.close()
 
@@ -434,6 +435,36 @@ def batched(torch, dev, ctx, w, n, flush, count=8, reps=20):
             "batch_e2e_h_per_s": count * (reps // 2) / e2e_s}
 
 
+def other_domains(torch, dev, g3h, synth, flush, steps=200):
+    """H/s on the other three proving-key-shaped domains (2^12, 2^14, 2^17), timed like
+    the headline: device buffers, L2 flushed between steps outside the events."""
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for k in (12, 14, 17):
+        A, B, w = synth.problem(k)
+        n = 1 << k
+        ctx = g3h.Context(k, w.shape[0], A, B, device=dev.index)
+        wd = torch.from_numpy(w.view(np.int32)).to(dev)
+        hm = torch.empty((n, 8), dtype=torch.int32, device=dev)
+        hs = torch.empty_like(hm)
+        for _ in range(5):
+            ctx.compute_h(wd, hm, hs)
+        evs = []
+        for i in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ctx.compute_h(wd, hm, hs)
+            e1.record(stream)
+            evs.append((e0, e1))
+            flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        ctx.close()
+        out["h_per_s_2^%d" % k] = 1e3 / ms
+        out["ms_per_h_2^%d" % k] = ms
+    return out
+
+
 def stress_2_22(torch, dev, g3h, synth):
     """Secondary figures on the 2^22 stress vectors (inputs larger than L2): one forward
     coset NTT (Fr NTT Gelem/s) and the H path on given a, b, c = a*b."""
@@ -466,11 +497,21 @@ def stress_2_22(torch, dev, g3h, synth):
 
     ntt_ms = timed(lambda: ctx.ntt(x, coset=True))
     h_ms = timed(lambda: ctx.compute_h_abc(ad, bd, cd, hm, hs))
+    # the witness copy to standard form (HBM-bound: 32 bytes read + 32 written per
+    # element) on 2^24 elements, 4x the L2 each way
+    del x, hm, hs
+    big = torch.cat([ad, bd, cd, ad])
+    big_out = torch.empty_like(big)
+    m2s_ms = timed(lambda: ctx.mont_to_std(big, big_out))
+    m2s_gbs = 64 * big.shape[0] / (m2s_ms * 1e-3) / 1e9
     ctx.sync()
     ctx.close()
+    peak = float(measured_peaks().get("hbm_gbs", 0.0)) or None
     return {"ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,
             "h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
-            "ntt_gelem_s_2^22_in_h": 6 * n / (h_ms * 1e-3) / 1e9}
+            "ntt_gelem_s_2^22_in_h": 6 * n / (h_ms * 1e-3) / 1e9,
+            "mont_to_std_2^24_ms": m2s_ms, "mont_to_std_2^24_gb_s": m2s_gbs,
+            "mont_to_std_2^24_frac_of_measured_hbm": m2s_gbs / peak if peak else None}
 
 
 if __name__ == "__main__":

@@ -126,6 +126,7 @@ void free_lane_streams(Lane& l) {
 
 struct g3h_ctx {
   int device = 0;
+  int sm_count = 1;
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   uint32_t log_n = 0, n_wires = 0;
@@ -637,6 +638,11 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
   g3h_ctx* c = new (std::nothrow) g3h_ctx();
   if (!c) return G3H_E_NOMEM;
   c->device = device;
+  if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) !=
+      cudaSuccess) {
+    delete c;
+    return G3H_E_CUDA;
+  }
   c->log_n = log_n;
   c->n = n;
   c->n_wires = n_wires;
@@ -928,6 +934,29 @@ int g3h_mul(g3h_ctx* c, const uint32_t* a, const uint32_t* b, uint32_t* out, siz
   if (rc == G3H_OK) rc = h2d(c, in + count, b, count * sizeof(fr_t));
   if (rc == G3H_OK) rc = launch(in, in + count, in + 2 * count);
   if (rc == G3H_OK) rc = d2h(c, out, in + 2 * count, count * sizeof(fr_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
+int g3h_mont_to_std(g3h_ctx* c, const uint32_t* in, uint32_t* out, size_t count,
+                    uint32_t flags) {
+  if (!c || ((!in || !out) && count)) return G3H_E_INVAL;
+  if (count == 0) return G3H_OK;
+  DeviceGuard guard(c->device);
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  auto launch = [&](const fr_t* x, fr_t* o) {
+    const size_t blocks = std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
+    return run(c, "mont_to_std", [&] {
+      k_mont_to_std<<<(unsigned)blocks, 256, 0, c->stream>>>(x, o, count, check, c->d_err);
+    });
+  };
+  if (flags & G3H_DEVICE_PTRS) return launch((const fr_t*)in, (fr_t*)out);
+  int rc = ensure_stage(c, count);
+  if (rc != G3H_OK) return rc;
+  fr_t* buf = c->d_stage;
+  rc = h2d(c, buf, in, count * sizeof(fr_t));
+  if (rc == G3H_OK) rc = launch(buf, buf);
+  if (rc == G3H_OK) rc = d2h(c, out, buf, count * sizeof(fr_t));
   const int rc2 = finish(c);
   return rc != G3H_OK ? rc : rc2;
 }

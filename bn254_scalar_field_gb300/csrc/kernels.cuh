@@ -130,6 +130,21 @@ __global__ void __launch_bounds__(256) k_mul(const fr_t* a, const fr_t* b, fr_t*
   fr_store(out + i, fr_canon(fr_mul(x, y)));
 }
 
+// Montgomery to standard form, elementwise (POINTWISE_CU, g16_mont_to_std: the witness is
+// uploaded once in Montgomery form for the gather and its standard-form copy, which the
+// MSM digit decomposition reads, is made on the device). out may equal in. A canonical
+// input gives a canonical output (REDC of a < r is < r). HBM-bound: 64 bytes per element
+// against 136 IMAD. Launch: a grid-stride loop, any grid (a multiple of the SM count).
+__global__ void __launch_bounds__(256) k_mont_to_std(const fr_t* in, fr_t* out, size_t n,
+                                                     uint32_t check, uint32_t* err) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const fr_t x = fr_load(in + i);
+    if (check) check_canonical(x, err);
+    fr_store(out + i, fr_from_mont(x));
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // Domains of at most 2^5 points: one block of 32 threads, every pass a loop over
 // butterflies through shared memory (the plain radix-2 schedule; such domains are too

@@ -35,7 +35,7 @@ CUDA_STREAM_LEGACY = 0x1
 ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather", "g3h_ntt",
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
                 "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
-                "g3h_compute_h_batch")
+                "g3h_compute_h_batch", "g3h_mont_to_std")
 
 
 class G3HError(RuntimeError):
@@ -74,6 +74,7 @@ def lib():
         L.g3h_ntt.argtypes = [P, P, I, I, U]
         L.g3h_join.argtypes = [P, P, P, P, P, P, U]
         L.g3h_mul.argtypes = [P, P, P, P, S, U]
+        L.g3h_mont_to_std.argtypes = [P, P, P, S, U]
         L.g3h_sync.argtypes = [P]
         L.g3h_destroy.argtypes = [P]
         L.g3h_destroy.restype = None
@@ -217,6 +218,16 @@ def g3h_mul(ctx, a, b, out, flags=0):
     _check(lib().g3h_mul(ctx, bufs[0][0], bufs[1][0], bufs[2][0], _elems(out), f), "g3h_mul")
 
 
+def g3h_mont_to_std(ctx, x, out, flags=0):
+    """out = x in standard form (x Montgomery); out may be x itself."""
+    if _elems(x) != _elems(out):
+        raise ValueError("x and out differ in length")
+    bufs = [_ptr(v, None) for v in (x, out)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_mont_to_std(ctx, bufs[0][0], bufs[1][0], _elems(out), f),
+           "g3h_mont_to_std")
+
+
 def g3h_sync(ctx):
     _check(lib().g3h_sync(ctx), "g3h_sync")
 
@@ -294,6 +305,9 @@ class Context:
 
     def mul(self, a, b, out, flags=0):
         g3h_mul(self.handle, a, b, out, flags)
+
+    def mont_to_std(self, x, out, flags=0):
+        g3h_mont_to_std(self.handle, x, out, flags)
 
     def sync(self):
         g3h_sync(self.handle)

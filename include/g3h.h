@@ -149,6 +149,16 @@ int g3h_join(g3h_ctx* ctx, const uint32_t* ea, const uint32_t* eb, const uint32_
 int g3h_mul(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, uint32_t* out, size_t count,
             uint32_t flags);
 
+/* out_i = in_i * R^-1 mod r for i < count: Montgomery form to standard form, the integer
+ * in [0, r) (POINTWISE_CU g16_mont_to_std, the witness path's step before the MSMs: the
+ * witness is uploaded once in Montgomery form for the gather, and its standard-form copy
+ * for the MSM window digits is made on the device). in and out may be the same buffer
+ * (converted in place); otherwise they must not overlap. Inputs must be canonical. Any
+ * count; independent of the context's domain (count may exceed 2^log_n). With host
+ * pointers the context's staging buffer grows to count elements. */
+int g3h_mont_to_std(g3h_ctx* ctx, const uint32_t* in, uint32_t* out, size_t count,
+                    uint32_t flags);
+
 /* Steps 2-5 like g3h_compute_h_abc, for callers that cannot allocate device memory: a
  * framework whose caching allocator must own every device byte, code running while its
  * stream is being captured into a CUDA graph (cudaMalloc is not permitted there), or a

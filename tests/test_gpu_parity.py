@@ -71,6 +71,37 @@ def test_mul_edge_and_random_values():
     assert np.array_equal(out, oracle.fr_mul_vec(a, b))
 
 
+@pytest.mark.parametrize("count", [0, 1, 7, 4099, (1 << 22) + 5])
+def test_mont_to_std(count):
+    """Montgomery to standard form, host and device buffers, out of place and in place;
+    counts ragged against the grid and one larger than L2."""
+    x = np.concatenate([_edge_fr(), synth.uniform_fr(synth.SplitMix64(5 + count), count)])[:count]
+    want = oracle.from_mont(x) if count else x.copy()
+    with g3h.Context(3) as ctx:
+        out = _zeros(count)
+        ctx.mont_to_std(x, out)
+        assert np.array_equal(out, want)
+        d = _dev(x)
+        ctx.mont_to_std(d, d)
+        ctx.sync()
+        assert np.array_equal(_host(d).reshape(-1, 8), want)
+
+
+def test_mont_to_std_rejects_noncanonical():
+    from oracle import fr_int as F
+
+    x = synth.uniform_fr(synth.SplitMix64(9), 1000)
+    x[517] = F.ints_to_array([F.R_MOD])[0]
+    with g3h.Context(3) as ctx:
+        with pytest.raises(g3h.G3HError) as e:
+            ctx.mont_to_std(x, _zeros(1000))
+        assert e.value.code == g3h.G3H_E_NONCANON
+        out = _zeros(1000)
+        x[517] = 0
+        ctx.mont_to_std(x, out)
+        assert np.array_equal(out, oracle.from_mont(x))
+
+
 # ---------------------------------------------------------------------- transforms ----
 
 NTT_SIZES = list(range(0, 13)) + [13, 14, 16, 17, 18]
