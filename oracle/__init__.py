@@ -4,12 +4,15 @@ TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the b
 CPU-baseline leg may import this package. The library (``bn254_scalar_field_gb300``) never
 does, and shares no code with it.
 
-Two independent implementations live here:
-  * ``fr_int``: pure-Python ints in standard form (small domains only);
-  * ``g3h_oracle.c``: plain C with four 64-bit limbs, built by :func:`build` into
-    ``oracle/_build/liboracle.so`` and called through ctypes by the wrappers below.
+Two independent implementations live here for each part:
+  * ``fr_int`` (quotient path) and ``g1_int`` (G1 multi-scalar multiplication): pure-Python
+    ints in standard form (small sizes only);
+  * ``g3h_oracle.c`` and ``g1_oracle.c``: plain C with four 64-bit limbs, built by
+    :func:`build` into ``oracle/_build/liboracle.so`` and called through ctypes by the
+    wrappers below.
 Array arguments are numpy uint32 arrays of shape (m, 8): eight little-endian limbs per
-element, Montgomery form (R = 2^256), as the library's boundary uses.
+element, Montgomery form (R = 2^256), as the library's boundary uses; G1 points are
+(m, 16) (affine x then y, infinity all zero), MSM scalars (m, 8) in standard form.
 """
 import ctypes
 import os
@@ -18,7 +21,7 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "g3h_oracle.c")
+_SRCS = [os.path.join(_HERE, "g3h_oracle.c"), os.path.join(_HERE, "g1_oracle.c")]
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lib = None
@@ -27,11 +30,12 @@ _lib = None
 def build(force=False):
     """Compile the C oracle with gcc (-O2, portable: no -march flags). Returns the path."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    fresh = os.path.exists(_LIB_PATH) and all(
+        os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)
     if force or not fresh:
         tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
         subprocess.check_call(
-            ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC])
+            ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-Wall", "-o", tmp] + _SRCS)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -59,6 +63,13 @@ def lib():
         L.orc_compute_h.restype = ctypes.c_int
         L.orc_compute_h_abc.argtypes = [U, P, P, P, P, P]
         L.orc_compute_h_abc.restype = ctypes.c_int
+        L.orc_fq_mul.argtypes = [P, P, P]
+        L.orc_fq_inv.argtypes = [P, P]
+        for name, args in (("orc_g1_on_curve", [P]), ("orc_g1_add", [P, P, P]),
+                           ("orc_g1_mul", [P, P, P]), ("orc_g1_msm", [S, P, P, P]),
+                           ("orc_g1_jacobian_to_affine", [P, P])):
+            getattr(L, name).argtypes = args
+            getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -184,3 +195,68 @@ def compute_h_abc(log_n, a, b, c):
     hs = np.zeros((n, 8), np.uint32)
     _check(lib().orc_compute_h_abc(log_n, _p(a), _p(b), _p(c), _p(hm), _p(hs)), "compute_h_abc")
     return hm, hs
+
+
+# ------------------------------------------------------------------------- G1 ----
+
+def _pts(a):
+    a = np.ascontiguousarray(a, dtype=np.uint32)
+    return a.reshape(-1, 16)
+
+
+def fq_mul(a, b):
+    """Montgomery product over F_q, elementwise on (m, 8) arrays."""
+    a, b = _fr(a), _fr(b)
+    out = np.empty_like(a)
+    for i in range(a.shape[0]):
+        lib().orc_fq_mul(_p(a[i]), _p(b[i]), _p(out[i]))
+    return out
+
+
+def fq_inv(a):
+    a = _fr(a)
+    out = np.empty_like(a)
+    for i in range(a.shape[0]):
+        lib().orc_fq_inv(_p(a[i]), _p(out[i]))
+    return out
+
+
+def g1_on_curve(points):
+    """Per point: on y^2 = x^3 + 3 with canonical coordinates, or the all-zero infinity."""
+    pts = _pts(points)
+    return np.array([bool(lib().orc_g1_on_curve(_p(pts[i]))) for i in range(pts.shape[0])])
+
+
+def g1_add(p, q):
+    p, q = _pts(p), _pts(q)
+    out = np.empty_like(p)
+    for i in range(p.shape[0]):
+        lib().orc_g1_add(_p(p[i]), _p(q[i]), _p(out[i]))
+    return out
+
+
+def g1_mul(points, scalars):
+    """scalars[i] * points[i] (scalars in standard form), affine."""
+    pts, k = _pts(points), _fr(scalars)
+    out = np.empty_like(pts)
+    for i in range(pts.shape[0]):
+        lib().orc_g1_mul(_p(pts[i]), _p(k[i]), _p(out[i]))
+    return out
+
+
+def g1_msm(points, scalars):
+    """sum_i scalars[i] * points[i] as one affine point, shape (16,)."""
+    pts, k = _pts(points), _fr(scalars)
+    if pts.shape[0] != k.shape[0]:
+        raise ValueError("points and scalars differ in length")
+    out = np.zeros(16, np.uint32)
+    lib().orc_g1_msm(pts.shape[0], _p(pts), _p(k), _p(out))
+    return out
+
+
+def g1_jacobian_to_affine(jac):
+    """The affine point (16 limbs) of a Jacobian point (24 limbs X, Y, Z)."""
+    j = np.ascontiguousarray(jac, dtype=np.uint32).reshape(24)
+    out = np.zeros(16, np.uint32)
+    lib().orc_g1_jacobian_to_affine(_p(j), _p(out))
+    return out
