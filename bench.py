@@ -378,6 +378,7 @@ def main():
     extra = {"ntt_gelem_s_2^18_in_h": 6 * n / (step_ms / args.steps * 1e-3) / 1e9}
     extra.update(batched(torch, dev, ctx, w, n, flush))
     if not args.no_extra and rank == 0:
+        extra.update(h_msm(torch, dev, g3h, flush))
         extra.update(other_domains(torch, dev, g3h, synth, flush))
         extra.update(stress_2_22(torch, dev, g3h, synth))
     ctx.close()
@@ -433,6 +434,55 @@ def batched(torch, dev, ctx, w, n, flush, count=8, reps=20):
         e2e_s += time.perf_counter() - t
     return {"batch_count": count, "batch_h_per_s": count * reps / (ms * 1e-3),
             "batch_e2e_h_per_s": count * (reps // 2) / e2e_s}
+
+
+MSM_OPS_PER_MADD = (8 + 2) * OPS_PER_MM  # madd-2008-s: 8 multiplies + 2 squarings
+
+
+def h_msm(torch, dev, g3h, flush, steps=50):
+    """The H multiexp at 2^18 (sum of h_i P_i over G1, h uniform in [0, r), bases sampled
+    on the curve): device buffers, bases prepared once (untimed), L2 flushed between
+    steps. Roofline of the bucket accumulation: one mixed addition per nonzero window
+    digit (16 per scalar), 10 Montgomery multiplies each."""
+    from bn254_scalar_field_gb300 import synth_g1
+
+    k = LOG_N
+    n = 1 << k
+    pts = synth_g1.points(n, seed=synth_g1.default_seed(k))
+    sc = synth_g1.scalars(n, seed=synth_g1.default_seed(k) + 1)
+    ctx = g3h.Context(0, device=dev.index)
+    ctx.msm_prepare(torch.from_numpy(pts.view(np.int32)).to(dev))
+    sd = torch.from_numpy(sc.view(np.int32)).to(dev)
+    res = torch.zeros(24, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        ctx.msm(sd, res)
+    evs = []
+    for i in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.fill_(i & 0xFF)
+        e0.record(stream)
+        ctx.msm(sd, res)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    ctx.timing_enable(True)
+    for i in range(10):
+        flush.fill_(i & 0xFF)
+        ctx.msm(sd, res)
+    kt = ctx.timing_read()
+    ctx.timing_enable(False)
+    ctx.sync()
+    ctx.close()
+    entries = 16 * n  # nonzero digits: all but about 2^-16 of them
+    acc_ms = kt["msm_accumulate"][1] / kt["msm_accumulate"][0]
+    peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    achieved = entries * MSM_OPS_PER_MADD / (acc_ms * 1e-3)
+    return {"msm_2^18_ms": ms, "msm_2^18_per_s": 1e3 / ms,
+            "msm_2^18_kernels_ms": {k2: v[1] / v[0] for k2, v in kt.items()},
+            "msm_accumulate_t_imad_s": achieved / 1e12,
+            "msm_accumulate_frac_of_derived_imad_peak": achieved / peak}
 
 
 def other_domains(torch, dev, g3h, synth, flush, steps=200):

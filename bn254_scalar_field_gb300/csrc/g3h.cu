@@ -20,6 +20,7 @@
 
 #include "../../include/g3h.h"
 #include "kernels.cuh"
+#include "msm.cuh"
 
 using namespace g3h;
 
@@ -160,6 +161,19 @@ struct g3h_ctx {
   std::vector<Graph> graphs;
   std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
   cudaEvent_t batch_start = nullptr;
+  // multi-scalar multiplication over G1 (g3h_msm_prepare / g3h_msm)
+  uint32_t msm_n = 0;                   // bases prepared
+  uint32_t msm_slots = 0;               // resident threads of k_msm_accumulate
+  g1_aff_t* d_msm_table = nullptr;      // 16 per base: 2^(16 w) P_i
+  uint32_t* d_msm_entries = nullptr;    // 16 per base
+  uint32_t* d_msm_counts = nullptr;     // per bucket
+  uint32_t* d_msm_offsets = nullptr;    // per bucket + 1
+  uint32_t* d_msm_cursor = nullptr;     // per bucket
+  g1_xyzz_t* d_msm_buckets = nullptr;   // per bucket
+  g1_xyzz_t* d_msm_spill = nullptr;     // head | tail parts, (n + 1) each
+  g1_xyzz_t* d_msm_groups = nullptr;    // U | V, kMsmGroups each
+  g1_xyzz_t* d_msm_parts = nullptr;     // kMsmParts
+  fq_t* d_msm_result = nullptr;         // Jacobian X, Y, Z
   bool timing = false;
   std::vector<TimedLaunch> launches;
   std::vector<cudaEvent_t> event_pool;
@@ -174,7 +188,21 @@ int dalloc(T** p, size_t count) {
   return cudaMalloc((void**)p, count * sizeof(T)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
 }
 
+void msm_free(g3h_ctx* c) {
+  void* bufs[] = {c->d_msm_table,   c->d_msm_entries, c->d_msm_counts, c->d_msm_offsets,
+                  c->d_msm_cursor,  c->d_msm_buckets, c->d_msm_spill,  c->d_msm_groups,
+                  c->d_msm_parts,   c->d_msm_result};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  c->d_msm_table = nullptr;
+  c->d_msm_entries = c->d_msm_counts = c->d_msm_offsets = c->d_msm_cursor = nullptr;
+  c->d_msm_buckets = c->d_msm_spill = c->d_msm_groups = c->d_msm_parts = nullptr;
+  c->d_msm_result = nullptr;
+  c->msm_n = 0;
+}
+
 void release(g3h_ctx* c) {
+  msm_free(c);
   void* bufs[] = {c->d_rpa,      c->d_cola,     c->d_rpb,      c->d_colb,        c->d_vala,
                   c->d_valb,     c->d_consts,   c->d_tw_fwd,   c->d_tw_inv,      c->d_shift_br,
                   c->d_coset_fwd, c->d_coset_inv, c->d_abc,    c->d_stage,       c->d_err,
@@ -302,10 +330,11 @@ int finish(g3h_ctx* c) {
       cudaStreamSynchronize(c->stream) != cudaSuccess)
     return G3H_E_CUDA;
   if (*c->h_err) {
+    const uint32_t e = *c->h_err;
     *c->h_err = 0;
     if (cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->stream) != cudaSuccess)
       return G3H_E_CUDA;
-    return G3H_E_NONCANON;
+    return (e & kMsmErrPoint) ? G3H_E_POINT : G3H_E_NONCANON;
   }
   return G3H_OK;
 }
@@ -961,6 +990,138 @@ int g3h_mont_to_std(g3h_ctx* c, const uint32_t* in, uint32_t* out, size_t count,
   return rc != G3H_OK ? rc : rc2;
 }
 
+// ---------------------------------------------------------------------------------------
+// Multi-scalar multiplication over G1.
+
+int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t check) {
+  cudaStream_t st = c->stream;
+  if (cudaMemsetAsync(c->d_msm_counts, 0, kMsmBuckets * sizeof(uint32_t), st) != cudaSuccess)
+    return G3H_E_CUDA;
+  const unsigned grid = (unsigned)std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
+  int rc = run(c, "msm_count", [&] {
+    k_msm_count<<<grid, 256, 0, st>>>(s, count, c->d_msm_counts, check, c->d_err);
+  });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_scan", [&] {
+      k_msm_scan<<<1, 1024, 0, st>>>(c->d_msm_counts, c->d_msm_offsets, c->d_msm_cursor);
+    });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_scatter", [&] {
+      k_msm_scatter<<<grid, 256, 0, st>>>(s, count, c->d_msm_cursor, c->d_msm_entries);
+    });
+  // slices of equal length, about one per resident thread of the accumulation kernel
+  const uint64_t max_entries = (uint64_t)count * kMsmWindows;
+  const uint32_t slice = (uint32_t)std::max<uint64_t>(
+      16, (max_entries + c->msm_slots - 1) / std::max<uint32_t>(c->msm_slots, 1));
+  const uint32_t n_slices = (uint32_t)((max_entries + slice - 1) / slice);
+  g1_xyzz_t* head = c->d_msm_spill;
+  g1_xyzz_t* tail = c->d_msm_spill + c->msm_n + 1;
+  if (rc == G3H_OK)
+    rc = run(c, "msm_accumulate", [&] {
+      k_msm_accumulate<<<blocks_for(n_slices, 256), 256, 0, st>>>(
+          c->d_msm_entries, c->d_msm_offsets, c->d_msm_table, c->d_msm_buckets, head, tail,
+          slice, n_slices);
+    });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_merge", [&] {
+      k_msm_merge<<<kMsmBuckets / 256, 256, 0, st>>>(c->d_msm_offsets, c->d_msm_buckets, head,
+                                                      tail, slice);
+    });
+  g1_xyzz_t* U = c->d_msm_groups;
+  g1_xyzz_t* V = c->d_msm_groups + kMsmGroups;
+  if (rc == G3H_OK)
+    rc = run(c, "msm_reduce_groups", [&] {
+      k_msm_reduce_groups<<<kMsmGroups / 256, 256, 0, st>>>(c->d_msm_buckets, U, V);
+    });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_reduce_bits", [&] {
+      k_msm_reduce_bits<<<kMsmParts, kMsmReduceThreads, kMsmReduceThreads * sizeof(g1_xyzz_t),
+                          st>>>(U, V, c->d_msm_parts);
+    });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_final", [&] { k_msm_final<<<1, 32, 0, st>>>(c->d_msm_parts, out); });
+  return rc;
+}
+
+int g3h_msm_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_t flags) {
+  if (!c || (!bases && n_bases)) return G3H_E_INVAL;
+  if (n_bases > (1u << G3H_MSM_MAX_LOG)) return G3H_E_RANGE;
+  DeviceGuard guard(c->device);
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
+  msm_free(c);
+  if (n_bases == 0) return G3H_OK;
+  const size_t n = n_bases;
+  int rc = dalloc(&c->d_msm_table, n * kMsmWindows);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_entries, n * kMsmWindows);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_counts, kMsmBuckets);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_offsets, kMsmBuckets + 1);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_cursor, kMsmBuckets);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_buckets, kMsmBuckets);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_spill, 2 * (n + 1));
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_groups, 2 * kMsmGroups);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_parts, kMsmParts);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_result, 3);
+  int per_sm = 0;
+  if (rc == G3H_OK &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_msm_accumulate, 256, 0) !=
+           cudaSuccess ||
+       cudaFuncSetAttribute((const void*)k_msm_reduce_bits,
+                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            (int)(kMsmReduceThreads * sizeof(g1_xyzz_t))) != cudaSuccess))
+    rc = G3H_E_CUDA;
+  c->msm_slots = (uint32_t)std::max(per_sm, 1) * 256u * (uint32_t)c->sm_count;
+  g1_aff_t* src = (g1_aff_t*)bases;
+  g1_aff_t* tmp = nullptr;
+  if (rc == G3H_OK && !(flags & G3H_DEVICE_PTRS)) {
+    rc = dalloc(&tmp, n);
+    if (rc == G3H_OK) rc = h2d(c, tmp, bases, n * sizeof(g1_aff_t));
+    src = tmp;
+  }
+  if (rc == G3H_OK)
+    rc = run(c, "msm_precompute", [&] {
+      k_msm_precompute<<<blocks_for(n, 128), 128, 0, c->stream>>>(src, n_bases, c->d_msm_table,
+                                                                  c->d_err);
+    });
+  const int rc2 = finish(c);
+  if (tmp) cudaFree(tmp);
+  if (rc == G3H_OK) rc = rc2;
+  if (rc != G3H_OK) {
+    msm_free(c);
+    return rc;
+  }
+  c->msm_n = n_bases;
+  return G3H_OK;
+}
+
+int g3h_msm(g3h_ctx* c, const uint32_t* scalars, uint32_t count, uint32_t* result,
+            uint32_t flags) {
+  if (!c || !result || (!scalars && count)) return G3H_E_INVAL;
+  if (count > c->msm_n) return G3H_E_RANGE;
+  DeviceGuard guard(c->device);
+  const bool dev = (flags & G3H_DEVICE_PTRS) != 0;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  if (count == 0) {  // the empty sum: infinity
+    if (dev)
+      return cudaMemsetAsync(result, 0, 3 * sizeof(fq_t), c->stream) == cudaSuccess ? G3H_OK
+                                                                                   : G3H_E_CUDA;
+    std::memset(result, 0, 3 * sizeof(fq_t));
+    return G3H_OK;
+  }
+  fq_t* out = dev ? (fq_t*)result : c->d_msm_result;
+  const fr_t* s = (const fr_t*)scalars;
+  int rc = G3H_OK;
+  if (!dev) {
+    rc = ensure_stage(c, count);
+    if (rc == G3H_OK) rc = h2d(c, c->d_stage, scalars, (size_t)count * sizeof(fr_t));
+    s = c->d_stage;
+  }
+  if (rc == G3H_OK) rc = msm_launches(c, s, count, out, check);
+  if (dev) return rc;
+  if (rc == G3H_OK) rc = d2h(c, result, out, 3 * sizeof(fq_t));
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
 int g3h_sync(g3h_ctx* c) {
   if (!c) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
@@ -983,6 +1144,7 @@ const char* g3h_strerror(int code) {
     case G3H_E_RANGE: return "value out of range (log_n, CSR row pointers or column index)";
     case G3H_E_NOMEM: return "out of memory";
     case G3H_E_CUDA: return "CUDA runtime error";
+    case G3H_E_POINT: return "a base point is not on the curve y^2 = x^3 + 3";
     default: return "unknown error";
   }
 }

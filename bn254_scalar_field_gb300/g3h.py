@@ -22,6 +22,7 @@ G3H_E_NONCANON = -2
 G3H_E_RANGE = -3
 G3H_E_NOMEM = -4
 G3H_E_CUDA = -5
+G3H_E_POINT = -6
 
 G3H_DEVICE_PTRS = 0x1
 G3H_NOCHECK = 0x2
@@ -29,13 +30,16 @@ G3H_FUSED_JOIN = 0x4
 G3H_SERIALIZE = 0x8
 G3H_NO_GRAPH = 0x10
 
+G3H_MAX_LOG_N = 27
+G3H_MSM_MAX_LOG = 24
+
 # cudaStreamLegacy: the runtime's handle for the legacy default stream.
 CUDA_STREAM_LEGACY = 0x1
 
 ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather", "g3h_ntt",
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
                 "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
-                "g3h_compute_h_batch", "g3h_mont_to_std")
+                "g3h_compute_h_batch", "g3h_mont_to_std", "g3h_msm_prepare", "g3h_msm")
 
 
 class G3HError(RuntimeError):
@@ -75,6 +79,8 @@ def lib():
         L.g3h_join.argtypes = [P, P, P, P, P, P, U]
         L.g3h_mul.argtypes = [P, P, P, P, S, U]
         L.g3h_mont_to_std.argtypes = [P, P, P, S, U]
+        L.g3h_msm_prepare.argtypes = [P, P, U, U]
+        L.g3h_msm.argtypes = [P, P, U, P, U]
         L.g3h_sync.argtypes = [P]
         L.g3h_destroy.argtypes = [P]
         L.g3h_destroy.restype = None
@@ -228,6 +234,29 @@ def g3h_mont_to_std(ctx, x, out, flags=0):
            "g3h_mont_to_std")
 
 
+def _words(x):
+    return x.numel() if _is_torch(x) else x.size
+
+
+def g3h_msm_prepare(ctx, bases, flags=0):
+    """Loads the G1 bases (n, 16) limbs: affine x, y in Montgomery form over F_q."""
+    if _words(bases) % 16:
+        raise ValueError("bases must hold 16 limbs per point")
+    bufs = [_ptr(bases, None)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_msm_prepare(ctx, bufs[0][0], _words(bases) // 16, f), "g3h_msm_prepare")
+
+
+def g3h_msm(ctx, scalars, result, flags=0):
+    """result (24 limbs: Jacobian X, Y, Z over F_q) = sum scalars[i] * base[i]; scalars
+    (count, 8) in standard form."""
+    if _words(result) != 24:
+        raise ValueError("result must hold 24 limbs")
+    bufs = [_ptr(v, None) for v in (scalars, result)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_msm(ctx, bufs[0][0], _elems(scalars), bufs[1][0], f), "g3h_msm")
+
+
 def g3h_sync(ctx):
     _check(lib().g3h_sync(ctx), "g3h_sync")
 
@@ -308,6 +337,12 @@ class Context:
 
     def mont_to_std(self, x, out, flags=0):
         g3h_mont_to_std(self.handle, x, out, flags)
+
+    def msm_prepare(self, bases, flags=0):
+        g3h_msm_prepare(self.handle, bases, flags)
+
+    def msm(self, scalars, result, flags=0):
+        g3h_msm(self.handle, scalars, result, flags)
 
     def sync(self):
         g3h_sync(self.handle)

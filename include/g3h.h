@@ -16,6 +16,9 @@
  * The 2^28-th root of unity is 5^((r-1)/2^28); omega = w^(2^(28-log_n)) and
  * g = w^(2^(27-log_n)).
  *
+ * Also here: the H multiexp of the next stage (MSM_CU, stage 9: sum_i h_i P_i over the
+ * BN254 curve group G1, with the standard-form h as scalars), g3h_msm_prepare / g3h_msm.
+ *
  * Layout. A field element is 32 bytes: eight little-endian uint32 limbs, least
  * significant limb first, no padding. "Montgomery" means the limbs hold x * 2^256 mod r
  * (arkworks' internal form, POINTWISE_CU "two output buffers"). Every input element must
@@ -27,7 +30,9 @@
  * place (pinned host memory makes the copies faster; pageable memory works). With
  * G3H_DEVICE_PTRS in `flags`, every data pointer of that call is a DEVICE pointer on the
  * context's device: the call only enqueues work on the context's stream and returns;
- * g3h_sync waits for it and reports errors found on the device. The caller owns every
+ * g3h_sync waits for it and reports errors found on the device. Device pointers must be
+ * 16-byte aligned (elements move as 16-byte vectors; cudaMalloc and torch allocations
+ * are). The caller owns every
  * buffer it passes; the context owns its tables, its copy of the CSR matrices and its
  * scratch vectors.
  *
@@ -56,6 +61,7 @@ extern "C" {
                                starting at 0, or a column index >= n_wires */
 #define G3H_E_NOMEM (-4)    /* device or pinned host allocation failed */
 #define G3H_E_CUDA (-5)     /* a CUDA runtime call failed (no device, launch error, ...) */
+#define G3H_E_POINT (-6)    /* a G1 base point is not on the curve y^2 = x^3 + 3 */
 
 /* flags */
 #define G3H_DEVICE_PTRS 0x1u  /* data pointers of this call are device pointers */
@@ -79,6 +85,7 @@ extern "C" {
                                  launch graph for these buffers and flags. Same results. */
 
 #define G3H_MAX_LOG_N 27
+#define G3H_MSM_MAX_LOG 24 /* at most 2^24 G1 bases per context */
 
 typedef struct g3h_ctx g3h_ctx;
 
@@ -159,6 +166,34 @@ int g3h_mul(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, uint32_t* out, s
 int g3h_mont_to_std(g3h_ctx* ctx, const uint32_t* in, uint32_t* out, size_t count,
                     uint32_t flags);
 
+/* ---- The H multiexp over G1 (MSM_CU, stage 9: Pippenger over BN254 G1, taking the
+ * standard-form h of g3h_compute_h as scalars) ----
+ *
+ * Curve y^2 = x^3 + 3 over F_q, q = 0x30644e72e131a029b85045b68181585d97816a916871ca8d3c
+ * 208c16d87cfd47 (alt_bn128 of EIP-196). A base is an affine point of 16 limbs: x then y,
+ * each eight little-endian 32-bit limbs in Montgomery form over F_q (x * 2^256 mod q),
+ * canonical (< q); (0, 0) stands for the point at infinity. */
+
+/* Loads n_bases G1 bases into the context (replacing any loaded before) and prepares them:
+ * for each base P the 16 points 2^(16 w) P, w < 16, are computed on the device and kept
+ * resident (1 KiB per base; 256 MiB for 2^18 bases), so that every later g3h_msm needs
+ * one bucket pass for all its windows. `bases`: 16 * n_bases limbs, host memory, or device
+ * memory with G3H_DEVICE_PTRS (read only during the call). n_bases <= 2^G3H_MSM_MAX_LOG.
+ * Synchronous. Returns G3H_E_NONCANON (a coordinate >= q), G3H_E_POINT (a base off the
+ * curve), G3H_E_RANGE, G3H_E_NOMEM; on error no bases are loaded. n_bases = 0 unloads. */
+int g3h_msm_prepare(g3h_ctx* ctx, const uint32_t* bases, uint32_t n_bases, uint32_t flags);
+
+/* result = sum_{i < count} s_i * P_i, P_i the first count loaded bases (count <= n_bases).
+ * scalars: 8 * count limbs, each scalar in standard form (the integer, < r; the h_std
+ * output of g3h_compute_h, not h_mont: a window digit of a Montgomery representative is a
+ * digit of s * R). result: 24 limbs, the sum in Jacobian coordinates (X, Y, Z),
+ * x = X / Z^2, y = Y / Z^3, each canonical Montgomery over F_q; the point at infinity is
+ * written as X = Y = Z = 0. Host pointers (synchronous) or, with G3H_DEVICE_PTRS, device
+ * pointers (asynchronous on the context's stream; errors at g3h_sync). Scalars >= r give
+ * G3H_E_NONCANON unless G3H_NOCHECK. count = 0 writes infinity. */
+int g3h_msm(g3h_ctx* ctx, const uint32_t* scalars, uint32_t count, uint32_t* result,
+            uint32_t flags);
+
 /* Steps 2-5 like g3h_compute_h_abc, for callers that cannot allocate device memory: a
  * framework whose caching allocator must own every device byte, code running while its
  * stream is being captured into a CUDA graph (cudaMalloc is not permitted there), or a
@@ -186,9 +221,9 @@ int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const uint32_t* 
                              const uint32_t* c, uint32_t* h_mont, uint32_t* h_std,
                              void* stream);
 
-/* Waits for all work enqueued on the context's stream; returns G3H_E_NONCANON if a
- * device-side input check failed since the last sync (and clears it), G3H_E_CUDA on a
- * CUDA error. */
+/* Waits for all work enqueued on the context's stream; returns G3H_E_NONCANON (or
+ * G3H_E_POINT) if a device-side input check failed since the last sync (and clears it),
+ * G3H_E_CUDA on a CUDA error. */
 int g3h_sync(g3h_ctx* ctx);
 
 /* Frees the context and everything it owns (waits for its stream first). NULL is a

@@ -41,9 +41,17 @@ def test_no_compute_symbols_missing_and_no_cpu_fallback():
 
 
 def test_strerror(L):
-    for code in (0, -1, -2, -3, -4, -5):
-        assert g3h.strerror(code)
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert g3h.strerror(code) != "unknown error"
     assert g3h.strerror(-99) == "unknown error"
+
+
+def test_header_constants_match_the_binding():
+    text = open(os.path.join(ROOT, "include", "g3h.h")).read()
+    consts = dict(re.findall(r"#define (G3H_\w+) \(?(-?(?:0x)?[0-9a-f]+)u?\)?", text))
+    for name, value in consts.items():
+        assert getattr(g3h, name) == int(value, 0), name
+    assert "G3H_E_POINT" in consts and "G3H_MSM_MAX_LOG" in consts
 
 
 def _rc(L, log_n, n_wires, A, B):
@@ -94,4 +102,7 @@ def test_null_context_calls(L):
     assert L.g3h_compute_h(None, None, None, None, 0) == g3h.G3H_E_INVAL
     assert L.g3h_ntt(None, None, 0, 0, 0) == g3h.G3H_E_INVAL
     assert L.g3h_info(None, None, None) == g3h.G3H_E_INVAL
+    assert L.g3h_mont_to_std(None, None, None, 0, 0) == g3h.G3H_E_INVAL
+    assert L.g3h_msm_prepare(None, None, 0, 0) == g3h.G3H_E_INVAL
+    assert L.g3h_msm(None, None, 0, None, 0) == g3h.G3H_E_INVAL
     L.g3h_destroy(None)
