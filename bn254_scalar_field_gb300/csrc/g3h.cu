@@ -171,8 +171,8 @@ struct g3h_ctx {
   uint32_t* d_msm_cursor = nullptr;     // per bucket
   g1_xyzz_t* d_msm_buckets = nullptr;   // per bucket
   g1_xyzz_t* d_msm_spill = nullptr;     // head | tail parts, (n + 1) each
-  g1_xyzz_t* d_msm_groups = nullptr;    // U | V, kMsmGroups each
-  g1_xyzz_t* d_msm_parts = nullptr;     // kMsmParts
+  g1_xyzz_t* d_msm_groups = nullptr;    // U | V, kMsmPairs each
+  g1_xyzz_t* d_msm_parts = nullptr;     // chunk sums (kMsmSumParts * kMsmChunks) | parts
   fq_t* d_msm_result = nullptr;         // Jacobian X, Y, Z
   bool timing = false;
   std::vector<TimedLaunch> launches;
@@ -1024,22 +1024,27 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_merge", [&] {
-      k_msm_merge<<<kMsmBuckets / 256, 256, 0, st>>>(c->d_msm_offsets, c->d_msm_buckets, head,
+      k_msm_merge<<<kMsmBuckets / 128, 128, 0, st>>>(c->d_msm_offsets, c->d_msm_buckets, head,
                                                       tail, slice);
     });
   g1_xyzz_t* U = c->d_msm_groups;
-  g1_xyzz_t* V = c->d_msm_groups + kMsmGroups;
+  g1_xyzz_t* V = c->d_msm_groups + kMsmPairs;
   if (rc == G3H_OK)
-    rc = run(c, "msm_reduce_groups", [&] {
-      k_msm_reduce_groups<<<kMsmGroups / 256, 256, 0, st>>>(c->d_msm_buckets, U, V);
+    rc = run(c, "msm_pairs", [&] {
+      k_msm_pairs<<<kMsmPairs / 128, 128, 0, st>>>(c->d_msm_buckets, U, V);
     });
   if (rc == G3H_OK)
-    rc = run(c, "msm_reduce_bits", [&] {
-      k_msm_reduce_bits<<<kMsmParts, kMsmReduceThreads, kMsmReduceThreads * sizeof(g1_xyzz_t),
-                          st>>>(U, V, c->d_msm_parts);
+    rc = run(c, "msm_part_chunks", [&] {
+      k_msm_part_chunks<<<dim3(kMsmChunks, kMsmSumParts), 256, 256 * sizeof(g1_xyzz_t), st>>>(
+          U, V, c->d_msm_parts);
+    });
+  g1_xyzz_t* parts = c->d_msm_parts + kMsmSumParts * kMsmChunks;
+  if (rc == G3H_OK)
+    rc = run(c, "msm_parts", [&] {
+      k_msm_parts<<<kMsmSumParts, 32, 0, st>>>(c->d_msm_parts, parts);
     });
   if (rc == G3H_OK)
-    rc = run(c, "msm_final", [&] { k_msm_final<<<1, 32, 0, st>>>(c->d_msm_parts, out); });
+    rc = run(c, "msm_final", [&] { k_msm_final<<<1, 32, 0, st>>>(parts, out); });
   return rc;
 }
 
@@ -1058,16 +1063,13 @@ int g3h_msm_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_cursor, kMsmBuckets);
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_buckets, kMsmBuckets);
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_spill, 2 * (n + 1));
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_groups, 2 * kMsmGroups);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_parts, kMsmParts);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_groups, 2 * kMsmPairs);
+  if (rc == G3H_OK) rc = dalloc(&c->d_msm_parts, kMsmSumParts * (kMsmChunks + 1));
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_result, 3);
   int per_sm = 0;
   if (rc == G3H_OK &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_msm_accumulate, 256, 0) !=
-           cudaSuccess ||
-       cudaFuncSetAttribute((const void*)k_msm_reduce_bits,
-                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            (int)(kMsmReduceThreads * sizeof(g1_xyzz_t))) != cudaSuccess))
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_msm_accumulate, 256, 0) !=
+          cudaSuccess)
     rc = G3H_E_CUDA;
   c->msm_slots = (uint32_t)std::max(per_sm, 1) * 256u * (uint32_t)c->sm_count;
   g1_aff_t* src = (g1_aff_t*)bases;

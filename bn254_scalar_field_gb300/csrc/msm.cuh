@@ -20,11 +20,10 @@
 //      leaves its part in that slice's head or tail slot (MSM_CU, "the load-balanced
 //      form": segmented accumulation with boundary spills);
 //   5. merge: a cut bucket sums its parts from the slices its run covers;
-//   6-8. the weighted sum sum_j j B_j: per group of 4 buckets (t = 0 .. 8191) the
-//      running sums give U_t = sum B and V_t = sum (j - 4t) B_j; then
-//      Q = sum_t V_t + sum_b 2^(b+2) sum_{t : bit b of t} U_t, thirteen bit-sums and one
-//      sum of V reduced by trees, scaled by doublings, and added in a last kernel, which
-//      writes Q in Jacobian coordinates.
+//   6-8. the weighted sum sum_j j B_j: per pair of buckets (t = 0 .. 16383) U_t and V_t;
+//      then Q = sum_t V_t + sum_b 2^(b+1) sum_{t : bit b of t} U_t, fourteen bit-sums and
+//      one sum of V reduced by trees over all SMs, scaled by doublings (one SM per part)
+//      and added in a last kernel, which writes Q in Jacobian coordinates.
 #pragma once
 #include "fr.cuh"
 #include "g1.cuh"
@@ -33,11 +32,6 @@ namespace g3h {
 
 constexpr uint32_t kMsmWindows = 16;          // windows of 16 bits
 constexpr uint32_t kMsmBuckets = 1u << 15;    // digit magnitudes 1 .. 2^15
-constexpr uint32_t kMsmGroup = 4;             // buckets per running-sum group
-constexpr uint32_t kMsmGroups = kMsmBuckets / kMsmGroup;  // 8192 = 2^13
-constexpr uint32_t kMsmGroupBits = 13;
-constexpr uint32_t kMsmParts = kMsmGroupBits + 1;  // 13 bit-sums of U, one sum of V
-constexpr uint32_t kMsmReduceThreads = 512;
 constexpr uint32_t kMsmErrPoint = 2u;  // error word bit: a base is not on the curve
 
 // Signed 16-bit digit w of the scalar s (eight 32-bit limbs), given the carry out of
@@ -107,46 +101,50 @@ __global__ void __launch_bounds__(256) k_msm_count(const fr_t* scalars, uint32_t
 }
 
 // Step 2: offsets[j] = sum of counts[0 .. j), offsets[kMsmBuckets] = total; cursor = offsets.
-// Launch: one block of 1024 threads (32 buckets per thread).
+// Warp w scans buckets [1024 w, 1024 w + 1024) as 32 rows of 32 (coalesced loads and
+// stores), then the 32 warp totals are scanned. Launch: one block of 1024 threads.
 __global__ void __launch_bounds__(1024) k_msm_scan(const uint32_t* counts, uint32_t* offsets,
                                                    uint32_t* cursor) {
-  constexpr uint32_t per = kMsmBuckets / 1024;
+  constexpr uint32_t rows = kMsmBuckets / 1024;  // per warp: rows of 32 buckets
   __shared__ uint32_t warp_tot[32];
-  const uint32_t t = threadIdx.x, lane = t & 31u, warp = t >> 5;
-  uint32_t local[per];
-  uint32_t sum = 0;
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t base = warp * 1024u;
+  uint32_t v[rows];
 #pragma unroll
-  for (uint32_t k = 0; k < per; k++) {
-    local[k] = counts[t * per + k];
-    sum += local[k];
-  }
-  // inclusive scan of the per-thread sums within the warp, then over the warps
-  uint32_t inc = sum;
+  for (uint32_t k = 0; k < rows; k++) v[k] = counts[base + k * 32u + lane];
+  uint32_t run = 0;  // this warp's total before row k
 #pragma unroll
-  for (uint32_t d = 1; d < 32; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc += o;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t v = warp_tot[lane];
+  for (uint32_t k = 0; k < rows; k++) {
+    uint32_t inc = v[k];
 #pragma unroll
     for (uint32_t d = 1; d < 32; d <<= 1) {
-      const uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
-      if (lane >= d) v += o;
+      const uint32_t o = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += o;
     }
-    warp_tot[lane] = v;  // inclusive over warps
+    const uint32_t row_total = __shfl_sync(0xffffffffu, inc, 31);
+    v[k] = run + inc - v[k];  // exclusive prefix within the warp's segment
+    run += row_total;
+  }
+  if (lane == 0) warp_tot[warp] = run;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = warp_tot[lane];
+    uint32_t inc = t;
+#pragma unroll
+    for (uint32_t d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += o;
+    }
+    warp_tot[lane] = inc - t;  // exclusive over the warps
+    if (lane == 31) offsets[kMsmBuckets] = inc;
   }
   __syncthreads();
-  uint32_t run = inc - sum + (warp ? warp_tot[warp - 1] : 0u);
+  const uint32_t off = warp_tot[warp];
 #pragma unroll
-  for (uint32_t k = 0; k < per; k++) {
-    offsets[t * per + k] = run;
-    cursor[t * per + k] = run;
-    run += local[k];
+  for (uint32_t k = 0; k < rows; k++) {
+    offsets[base + k * 32u + lane] = off + v[k];
+    cursor[base + k * 32u + lane] = off + v[k];
   }
-  if (t == 1023) offsets[kMsmBuckets] = run;
 }
 
 // Step 3. Launch: as k_msm_count.
@@ -213,10 +211,16 @@ __global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
   emit();
 }
 
+// The bucket sum below is a chain of dependent point operations on few threads: its time
+// is their latency, not throughput. Its kernels call these out-of-line copies, so that the
+// code each thread loops over stays small and resident in the instruction cache.
+__device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) { return xyzz_add(a, b); }
+__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl(a); }
+
 // Step 5: one thread per bucket. A bucket with no entries is set to infinity; a run cut by
 // slice boundaries is the tail part of its first slice plus the head parts of the rest.
-// Launch: kMsmBuckets / 256 blocks of 256.
-__global__ void __launch_bounds__(256) k_msm_merge(const uint32_t* offsets, g1_xyzz_t* buckets,
+// Launch: kMsmBuckets / 128 blocks of 128.
+__global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, g1_xyzz_t* buckets,
                                                    const g1_xyzz_t* head, const g1_xyzz_t* tail,
                                                    uint32_t slice) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -233,59 +237,103 @@ __global__ void __launch_bounds__(256) k_msm_merge(const uint32_t* offsets, g1_x
   buckets[j] = acc;
 }
 
-// Step 6: group t = buckets 4t .. 4t+3 (digits 4t+1 .. 4t+4): U_t = sum B,
-// V_t = sum_u (u + 1) B_{4t+u}, by running sums from the top. Launch: kMsmGroups / 256
-// blocks of 256.
-__global__ void __launch_bounds__(256) k_msm_reduce_groups(const g1_xyzz_t* buckets,
-                                                           g1_xyzz_t* U, g1_xyzz_t* V) {
+// The weighted sum Q = sum_j (j + 1) B_j. With pairs t = (B_2t, B_2t+1), digits 2t + 1 and
+// 2t + 2: U_t = B_2t + B_2t+1 and V_t = U_t + B_2t+1 = B_2t + 2 B_2t+1, so
+//   Q = sum_t (V_t + 2t U_t) = sum_t V_t + sum_{b < 14} 2^(b+1) sum_{t : bit b of t} U_t.
+// Part p < 14 is the sum over U_t with bit p of t set; part 14 is the sum of V.
+constexpr uint32_t kMsmPairs = kMsmBuckets / 2;          // 16384 = 2^14
+constexpr uint32_t kMsmPairBits = 14;
+constexpr uint32_t kMsmSumParts = kMsmPairBits + 1;      // 15
+constexpr uint32_t kMsmChunk = 512;                      // items per block in step 7
+constexpr uint32_t kMsmChunks = kMsmPairs / kMsmChunk;   // 32 (16 for the bit parts)
+
+// Step 6: U_t, V_t. Launch: kMsmPairs / 128 blocks of 128.
+__global__ void __launch_bounds__(128) k_msm_pairs(const g1_xyzz_t* buckets, g1_xyzz_t* U,
+                                                   g1_xyzz_t* V) {
   const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= kMsmGroups) return;
-  g1_xyzz_t run = xyzz_infinity(), acc = xyzz_infinity();
-  for (int u = (int)kMsmGroup - 1; u >= 0; u--) {
-    run = xyzz_add(run, buckets[t * kMsmGroup + (uint32_t)u]);
-    acc = xyzz_add(acc, run);
-  }
-  U[t] = run;
-  V[t] = acc;
+  if (t >= kMsmPairs) return;
+  const g1_xyzz_t hi = buckets[2 * t + 1];
+  const g1_xyzz_t u = xyzz_add_nl(buckets[2 * t], hi);
+  U[t] = u;
+  V[t] = xyzz_add_nl(u, hi);
 }
 
-// Step 7: block b < 13 sums U_t over the t with bit b set and doubles the sum b + 2 times
-// (the weight 4 t of U_t, bit by bit); block 13 sums V. Launch: kMsmParts blocks of
-// kMsmReduceThreads, kMsmReduceThreads * 128 bytes of dynamic shared memory.
-__global__ void __launch_bounds__(kMsmReduceThreads) k_msm_reduce_bits(const g1_xyzz_t* U,
-                                                                       const g1_xyzz_t* V,
-                                                                       g1_xyzz_t* parts) {
+// Step 7: partial sums of the parts, chunk c of part p = blockIdx (c, p): 512 items, two per
+// thread, then a tree in shared memory. The bit parts have 8192 items (16 chunks): item i
+// is t with bit p set, i.e. bit p inserted into i. Launch: grid (kMsmChunks, kMsmSumParts),
+// 256 threads, 256 * 128 bytes of dynamic shared memory.
+__global__ void __launch_bounds__(256) k_msm_part_chunks(const g1_xyzz_t* U, const g1_xyzz_t* V,
+                                                         g1_xyzz_t* partial) {
   extern __shared__ g1_xyzz_t sm_pts[];
-  const uint32_t b = blockIdx.x, tid = threadIdx.x;
-  g1_xyzz_t acc = xyzz_infinity();
-  for (uint32_t t = tid; t < kMsmGroups; t += kMsmReduceThreads) {
-    if (b < kMsmGroupBits) {
-      if ((t >> b) & 1u) acc = xyzz_add(acc, U[t]);
-    } else {
-      acc = xyzz_add(acc, V[t]);
+  const uint32_t c = blockIdx.x, p = blockIdx.y, tid = threadIdx.x;
+  const bool bit_part = p < kMsmPairBits;
+  if (bit_part && c >= kMsmChunks / 2) return;  // whole block exits together
+  g1_xyzz_t acc;
+  {
+    const uint32_t i0 = c * kMsmChunk + 2 * tid;
+    g1_xyzz_t x[2];
+#pragma unroll
+    for (int k = 0; k < 2; k++) {
+      const uint32_t i = i0 + (uint32_t)k;
+      if (bit_part) {
+        const uint32_t low = i & ((1u << p) - 1u);
+        const uint32_t t = ((i >> p) << (p + 1)) | (1u << p) | low;
+        x[k] = U[t];
+      } else {
+        x[k] = V[i];
+      }
     }
+    acc = xyzz_add_nl(x[0], x[1]);
   }
   sm_pts[tid] = acc;
   __syncthreads();
-  for (uint32_t s = kMsmReduceThreads / 2; s > 0; s >>= 1) {
-    if (tid < s) sm_pts[tid] = xyzz_add(sm_pts[tid], sm_pts[tid + s]);
+  for (uint32_t s = 128; s > 0; s >>= 1) {
+    if (tid < s) sm_pts[tid] = xyzz_add_nl(sm_pts[tid], sm_pts[tid + s]);
     __syncthreads();
   }
-  if (tid == 0) {
-    g1_xyzz_t p = sm_pts[0];
-    if (b < kMsmGroupBits)
-      for (uint32_t d = 0; d < b + 2; d++) p = xyzz_dbl(p);
-    parts[b] = p;
+  if (tid == 0) partial[p * kMsmChunks + c] = sm_pts[0];
+}
+
+__device__ __forceinline__ g1_xyzz_t xyzz_shfl_down(const g1_xyzz_t& p, uint32_t d) {
+  g1_xyzz_t o;
+#pragma unroll
+  for (int w = 0; w < 8; w++) {
+    o.x.v[w] = __shfl_down_sync(0xffffffffu, p.x.v[w], d);
+    o.y.v[w] = __shfl_down_sync(0xffffffffu, p.y.v[w], d);
+    o.zz.v[w] = __shfl_down_sync(0xffffffffu, p.zz.v[w], d);
+    o.zzz.v[w] = __shfl_down_sync(0xffffffffu, p.zzz.v[w], d);
+  }
+  return o;
+}
+
+// Step 8: block p (one warp, a block per part so that each runs on an SM of its own) sums
+// part p's chunks by shuffles and scales the sum: part p < 14 by 2^(p+1), p + 1 doublings.
+// Launch: kMsmSumParts blocks of 32.
+__global__ void __launch_bounds__(32) k_msm_parts(const g1_xyzz_t* partial, g1_xyzz_t* parts) {
+  const uint32_t lane = threadIdx.x, p = blockIdx.x;
+  const uint32_t n_chunks = p < kMsmPairBits ? kMsmChunks / 2 : kMsmChunks;
+  g1_xyzz_t acc = lane < n_chunks ? partial[p * kMsmChunks + lane] : xyzz_infinity();
+  for (uint32_t d = 16; d > 0; d >>= 1) {
+    const g1_xyzz_t o = xyzz_shfl_down(acc, d);
+    if (lane < d) acc = xyzz_add_nl(acc, o);
+  }
+  if (lane == 0) {
+    if (p < kMsmPairBits)
+      for (uint32_t k = 0; k <= p; k++) acc = xyzz_dbl_nl(acc);
+    parts[p] = acc;
   }
 }
 
-// Step 8: Q = sum of the parts, written as Jacobian (X, Y, Z), canonical Montgomery
-// coordinates, infinity as (0, 0, 0). Launch: one block of 32 (lane 0 works).
+// Step 9: Q = the sum of the 15 parts (shuffles), written in Jacobian coordinates,
+// canonical Montgomery, infinity as (0, 0, 0). Launch: one block of 32.
 __global__ void __launch_bounds__(32) k_msm_final(const g1_xyzz_t* parts, fq_t* out) {
-  if (threadIdx.x != 0) return;
-  g1_xyzz_t acc = xyzz_infinity();
-  for (uint32_t b = 0; b < kMsmParts; b++) acc = xyzz_add(acc, parts[b]);
-  xyzz_to_jacobian(acc, out[0], out[1], out[2]);
+  const uint32_t lane = threadIdx.x;
+  g1_xyzz_t acc = lane < kMsmSumParts ? parts[lane] : xyzz_infinity();
+  for (uint32_t d = 8; d > 0; d >>= 1) {
+    const g1_xyzz_t o = xyzz_shfl_down(acc, d);
+    if (lane < d) acc = xyzz_add_nl(acc, o);
+  }
+  if (lane == 0) xyzz_to_jacobian(acc, out[0], out[1], out[2]);
 }
 
 }  // namespace g3h
