@@ -22,6 +22,20 @@ struct __align__(16) g1_xyzz_t {
   fq_t x, y, zz, zzz;
 };
 
+// Which field multiplication the point formulas use: fq_mul inlined at every call, or one
+// out-of-line copy. A point addition inlines 14 multiplies (some 30 KB of code), more than
+// the instruction cache keeps; where few warps run, as in the bucket sum, they stall on
+// instruction fetch, and calling one compact multiply is faster.
+struct FqInline {
+  static __device__ __forceinline__ fq_t mul(const fq_t& a, const fq_t& b) { return fq_mul(a, b); }
+};
+__device__ __noinline__ fq_t fq_mul_call(fq_t a, fq_t b) { return fq_mul(a, b); }
+struct FqCall {
+  static __device__ __forceinline__ fq_t mul(const fq_t& a, const fq_t& b) {
+    return fq_mul_call(a, b);
+  }
+};
+
 __device__ __forceinline__ g1_xyzz_t xyzz_infinity() {
   g1_xyzz_t p;
   p.x = fq_zero();
@@ -52,32 +66,34 @@ __device__ __forceinline__ g1_xyzz_t xyzz_from_aff(const g1_aff_t& a) {
 //   X3 = M^2 - 2S, Y3 = M (S - X3) - W Y, ZZ3 = V ZZ, ZZZ3 = W ZZZ.
 // Infinity doubles to itself (V = W = 0 when ZZ = 0 keeps ZZ3 = 0); y = 0 does not occur
 // (the group has odd order r) but would give ZZ3 = 0, the right answer, too.
-__device__ __forceinline__ g1_xyzz_t xyzz_dbl(const g1_xyzz_t& p) {
+template <class M>
+__device__ __forceinline__ g1_xyzz_t xyzz_dbl_t(const g1_xyzz_t& p) {
   const fq_t u = fq_dbl(p.y);
-  const fq_t v = fq_sqr(u);
-  const fq_t w = fq_mul(u, v);
-  const fq_t s = fq_mul(p.x, v);
-  const fq_t xx = fq_sqr(p.x);
+  const fq_t v = M::mul(u, u);
+  const fq_t w = M::mul(u, v);
+  const fq_t s = M::mul(p.x, v);
+  const fq_t xx = M::mul(p.x, p.x);
   const fq_t m = fq_add(fq_dbl(xx), xx);
   g1_xyzz_t r;
-  r.x = fq_sub(fq_sqr(m), fq_dbl(s));
-  r.y = fq_sub(fq_mul(m, fq_sub(s, r.x)), fq_mul(w, p.y));
-  r.zz = fq_mul(v, p.zz);
-  r.zzz = fq_mul(w, p.zzz);
+  r.x = fq_sub(M::mul(m, m), fq_dbl(s));
+  r.y = fq_sub(M::mul(m, fq_sub(s, r.x)), M::mul(w, p.y));
+  r.zz = M::mul(v, p.zz);
+  r.zzz = M::mul(w, p.zzz);
   return r;
 }
 
 // 2P for an affine P (mdbl-2008-s-1: ZZ = ZZZ = 1, so ZZ3 = V, ZZZ3 = W).
-__device__ __forceinline__ g1_xyzz_t xyzz_mdbl(const g1_aff_t& p) {
+template <class M>
+__device__ __forceinline__ g1_xyzz_t xyzz_mdbl_t(const g1_aff_t& p) {
   const fq_t u = fq_dbl(p.y);
-  const fq_t v = fq_sqr(u);
-  const fq_t w = fq_mul(u, v);
-  const fq_t s = fq_mul(p.x, v);
-  const fq_t xx = fq_sqr(p.x);
+  const fq_t v = M::mul(u, u);
+  const fq_t w = M::mul(u, v);
+  const fq_t s = M::mul(p.x, v);
+  const fq_t xx = M::mul(p.x, p.x);
   const fq_t m = fq_add(fq_dbl(xx), xx);
   g1_xyzz_t r;
-  r.x = fq_sub(fq_sqr(m), fq_dbl(s));
-  r.y = fq_sub(fq_mul(m, fq_sub(s, r.x)), fq_mul(w, p.y));
+  r.x = fq_sub(M::mul(m, m), fq_dbl(s));
+  r.y = fq_sub(M::mul(m, fq_sub(s, r.x)), M::mul(w, p.y));
   r.zz = v;
   r.zzz = w;
   return r;
@@ -88,24 +104,25 @@ __device__ __forceinline__ g1_xyzz_t xyzz_mdbl(const g1_aff_t& p) {
 //   X3 = R^2 - PPP - 2Q, Y3 = R (Q - X3) - Y1 PPP, ZZ3 = ZZ1 PP, ZZZ3 = ZZZ1 PPP.
 // P = 0 means the same x: R = 0 is the same point (double b), else opposite points
 // (infinity).
-__device__ __forceinline__ g1_xyzz_t xyzz_madd(const g1_xyzz_t& acc, const g1_aff_t& b) {
+template <class M>
+__device__ __forceinline__ g1_xyzz_t xyzz_madd_t(const g1_xyzz_t& acc, const g1_aff_t& b) {
   if (xyzz_is_inf(acc)) return xyzz_from_aff(b);
-  const fq_t u2 = fq_mul(b.x, acc.zz);
-  const fq_t s2 = fq_mul(b.y, acc.zzz);
+  const fq_t u2 = M::mul(b.x, acc.zz);
+  const fq_t s2 = M::mul(b.y, acc.zzz);
   const fq_t p = fq_sub(u2, acc.x);
   const fq_t r = fq_sub(s2, acc.y);
   if (fq_is_zero(p)) {
-    if (fq_is_zero(r)) return xyzz_mdbl(b);
+    if (fq_is_zero(r)) return xyzz_mdbl_t<M>(b);
     return xyzz_infinity();
   }
-  const fq_t pp = fq_sqr(p);
-  const fq_t ppp = fq_mul(p, pp);
-  const fq_t q = fq_mul(acc.x, pp);
+  const fq_t pp = M::mul(p, p);
+  const fq_t ppp = M::mul(p, pp);
+  const fq_t q = M::mul(acc.x, pp);
   g1_xyzz_t o;
-  o.x = fq_sub(fq_sub(fq_sqr(r), ppp), fq_dbl(q));
-  o.y = fq_sub(fq_mul(r, fq_sub(q, o.x)), fq_mul(acc.y, ppp));
-  o.zz = fq_mul(acc.zz, pp);
-  o.zzz = fq_mul(acc.zzz, ppp);
+  o.x = fq_sub(fq_sub(M::mul(r, r), ppp), fq_dbl(q));
+  o.y = fq_sub(M::mul(r, fq_sub(q, o.x)), M::mul(acc.y, ppp));
+  o.zz = M::mul(acc.zz, pp);
+  o.zzz = M::mul(acc.zzz, ppp);
   return o;
 }
 
@@ -113,28 +130,37 @@ __device__ __forceinline__ g1_xyzz_t xyzz_madd(const g1_xyzz_t& acc, const g1_af
 //   U1 = X1 ZZ2, U2 = X2 ZZ1, S1 = Y1 ZZZ2, S2 = Y2 ZZZ1, P = U2 - U1, R = S2 - S1,
 //   PP = P^2, PPP = P PP, Q = U1 PP, X3 = R^2 - PPP - 2Q, Y3 = R (Q - X3) - S1 PPP,
 //   ZZ3 = ZZ1 ZZ2 PP, ZZZ3 = ZZZ1 ZZZ2 PPP.
-__device__ __forceinline__ g1_xyzz_t xyzz_add(const g1_xyzz_t& a, const g1_xyzz_t& b) {
+template <class M>
+__device__ __forceinline__ g1_xyzz_t xyzz_add_t(const g1_xyzz_t& a, const g1_xyzz_t& b) {
   if (xyzz_is_inf(a)) return b;
   if (xyzz_is_inf(b)) return a;
-  const fq_t u1 = fq_mul(a.x, b.zz);
-  const fq_t u2 = fq_mul(b.x, a.zz);
-  const fq_t s1 = fq_mul(a.y, b.zzz);
-  const fq_t s2 = fq_mul(b.y, a.zzz);
+  const fq_t u1 = M::mul(a.x, b.zz);
+  const fq_t u2 = M::mul(b.x, a.zz);
+  const fq_t s1 = M::mul(a.y, b.zzz);
+  const fq_t s2 = M::mul(b.y, a.zzz);
   const fq_t p = fq_sub(u2, u1);
   const fq_t r = fq_sub(s2, s1);
   if (fq_is_zero(p)) {
-    if (fq_is_zero(r)) return xyzz_dbl(a);
+    if (fq_is_zero(r)) return xyzz_dbl_t<M>(a);
     return xyzz_infinity();
   }
-  const fq_t pp = fq_sqr(p);
-  const fq_t ppp = fq_mul(p, pp);
-  const fq_t q = fq_mul(u1, pp);
+  const fq_t pp = M::mul(p, p);
+  const fq_t ppp = M::mul(p, pp);
+  const fq_t q = M::mul(u1, pp);
   g1_xyzz_t o;
-  o.x = fq_sub(fq_sub(fq_sqr(r), ppp), fq_dbl(q));
-  o.y = fq_sub(fq_mul(r, fq_sub(q, o.x)), fq_mul(s1, ppp));
-  o.zz = fq_mul(fq_mul(a.zz, b.zz), pp);
-  o.zzz = fq_mul(fq_mul(a.zzz, b.zzz), ppp);
+  o.x = fq_sub(fq_sub(M::mul(r, r), ppp), fq_dbl(q));
+  o.y = fq_sub(M::mul(r, fq_sub(q, o.x)), M::mul(s1, ppp));
+  o.zz = M::mul(M::mul(a.zz, b.zz), pp);
+  o.zzz = M::mul(M::mul(a.zzz, b.zzz), ppp);
   return o;
+}
+
+__device__ __forceinline__ g1_xyzz_t xyzz_dbl(const g1_xyzz_t& p) { return xyzz_dbl_t<FqInline>(p); }
+__device__ __forceinline__ g1_xyzz_t xyzz_madd(const g1_xyzz_t& acc, const g1_aff_t& b) {
+  return xyzz_madd_t<FqInline>(acc, b);
+}
+__device__ __forceinline__ g1_xyzz_t xyzz_add(const g1_xyzz_t& a, const g1_xyzz_t& b) {
+  return xyzz_add_t<FqInline>(a, b);
 }
 
 // The affine point of p, canonical coordinates; (0, 0) for infinity. One inversion:
@@ -155,19 +181,20 @@ __device__ __forceinline__ g1_aff_t xyzz_to_aff(const g1_xyzz_t& p) {
 
 // Jacobian (X', Y', Z') of p with x = X'/Z'^2, y = Y'/Z'^3: Z' = ZZ ZZZ,
 // X' = X ZZ ZZZ^2, Y' = Y ZZ^3 ZZZ^2 (no inversion); infinity as (0, 0, 0).
-__device__ __forceinline__ void xyzz_to_jacobian(const g1_xyzz_t& p, fq_t& X, fq_t& Y,
-                                                 fq_t& Z) {
+template <class M>
+__device__ __forceinline__ void xyzz_to_jacobian_t(const g1_xyzz_t& p, fq_t& X, fq_t& Y,
+                                                   fq_t& Z) {
   if (xyzz_is_inf(p)) {
     X = fq_zero();
     Y = fq_zero();
     Z = fq_zero();
     return;
   }
-  const fq_t z = fq_mul(p.zz, p.zzz);
-  const fq_t zzz2 = fq_sqr(p.zzz);
-  X = fq_canon(fq_mul(fq_mul(p.x, p.zz), zzz2));
-  const fq_t zz3 = fq_mul(fq_sqr(p.zz), p.zz);
-  Y = fq_canon(fq_mul(fq_mul(p.y, zz3), zzz2));
+  const fq_t z = M::mul(p.zz, p.zzz);
+  const fq_t zzz2 = M::mul(p.zzz, p.zzz);
+  X = fq_canon(M::mul(M::mul(p.x, p.zz), zzz2));
+  const fq_t zz3 = M::mul(M::mul(p.zz, p.zz), p.zz);
+  Y = fq_canon(M::mul(M::mul(p.y, zz3), zzz2));
   Z = fq_canon(z);
 }
 

@@ -212,10 +212,15 @@ __global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
 }
 
 // The bucket sum below is a chain of dependent point operations on few threads: its time
-// is their latency, not throughput. Its kernels call these out-of-line copies, so that the
-// code each thread loops over stays small and resident in the instruction cache.
-__device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) { return xyzz_add(a, b); }
-__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl(a); }
+// is their latency, not throughput, and with few warps per SM nothing hides instruction
+// fetch. Its kernels call these out-of-line copies, which call one out-of-line multiply,
+// so that the code each thread loops over stays small and resident in the instruction
+// cache.
+using FqTail = FqCall;
+__device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) {
+  return xyzz_add_t<FqTail>(a, b);
+}
+__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<FqTail>(a); }
 
 // Step 5: one thread per bucket. A bucket with no entries is set to infinity; a run cut by
 // slice boundaries is the tail part of its first slice plus the head parts of the rest.
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(32) k_msm_final(const g1_xyzz_t* parts, fq_t* 
     const g1_xyzz_t o = xyzz_shfl_down(acc, d);
     if (lane < d) acc = xyzz_add_nl(acc, o);
   }
-  if (lane == 0) xyzz_to_jacobian(acc, out[0], out[1], out[2]);
+  if (lane == 0) xyzz_to_jacobian_t<FqTail>(acc, out[0], out[1], out[2]);
 }
 
 }  // namespace g3h
