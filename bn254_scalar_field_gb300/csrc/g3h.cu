@@ -258,22 +258,40 @@ int run(g3h_ctx* c, const char* name, F&& launch) {
 
 unsigned blocks_for(size_t count, unsigned per) { return (unsigned)((count + per - 1) / per); }
 
-int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, void (*kern)(SliceArgs),
-                    const SliceArgs& a, unsigned nvec) {
-  const dim3 grid((unsigned)(c->n >> a.kk), nvec);
-  const dim3 block(std::min(1u << (a.kk - 1u), kSliceThreads));
-  const size_t smem = (size_t)32 << a.kk;
-  return run_on(c, st, name, [&] { kern<<<grid, block, smem, st>>>(a); });
+enum class Slice { dif, mid, dit, brev };
+
+// The build of a slice kernel for slices of 2^kk elements, and its threads per block: one
+// per butterfly of a radix-2 pass, one per group of four of a radix-4 pass pair, up to
+// the build's block size.
+void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
+  const bool r4 = kk >= kRadix4MinSliceBits && kk <= kRadix4MaxSliceBits && kk >= 2;
+  *threads = r4 ? std::min(1u << (kk - 2u), SliceCfg<1>::threads)
+                : std::min(1u << (kk - 1u), SliceCfg<0>::threads);
+  switch (which) {
+    case Slice::dif: return r4 ? k_ntt_dif<1> : k_ntt_dif<0>;
+    case Slice::mid: return r4 ? k_ntt_mid<1> : k_ntt_mid<0>;
+    case Slice::dit: return r4 ? k_ntt_dit<1> : k_ntt_dit<0>;
+    default: *threads = std::min(1u << (kk - 1u), kSliceThreads); return k_ntt_brev;
+  }
 }
 
-int launch_slice(g3h_ctx* c, const char* name, void (*kern)(SliceArgs), const SliceArgs& a,
-                 unsigned nvec) {
-  return launch_slice_on(c, c->stream, name, kern, a, nvec);
+int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, Slice which,
+                    const SliceArgs& a, unsigned nvec) {
+  uint32_t threads = 0;
+  void (*kern)(SliceArgs) = slice_kernel(which, a.kk, &threads);
+  const dim3 grid((unsigned)(c->n >> a.kk), nvec);
+  const size_t smem = (size_t)32 << a.kk;
+  return run_on(c, st, name, [&] { kern<<<grid, threads, smem, st>>>(a); });
+}
+
+int launch_slice(g3h_ctx* c, const char* name, Slice which, const SliceArgs& a, unsigned nvec) {
+  return launch_slice_on(c, c->stream, name, which, a, nvec);
 }
 
 int set_smem_limits() {
   const int bytes = 32 << 11;  // the largest slice, 2^11 elements
-  void (*kerns[])(SliceArgs) = {k_ntt_dif, k_ntt_mid, k_ntt_dit, k_ntt_brev};
+  void (*kerns[])(SliceArgs) = {k_ntt_dif<0>, k_ntt_mid<0>, k_ntt_dit<0>, k_ntt_dif<1>,
+                                k_ntt_mid<1>, k_ntt_dit<1>, k_ntt_brev};
   for (auto k : kerns)
     if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
@@ -438,7 +456,7 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
       x.mode = (first && check && !w) ? SL_CHECK : 0u;
       if (first && w) x.mode |= SL_C_FROM_AB;
       x.vbase = v;
-      rc = launch_slice_on(c, vs[v], "ntt_dif", k_ntt_dif, x, rows);
+      rc = launch_slice_on(c, vs[v], "ntt_dif", Slice::dif, x, rows);
     }
   }
   for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
@@ -450,7 +468,7 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
     x.kk = pl.kk[0];
     x.c0 = 0;
     x.vbase = v;
-    rc = launch_slice_on(c, vs[v], "ntt_mid", k_ntt_mid, x, rows);
+    rc = launch_slice_on(c, vs[v], "ntt_mid", Slice::mid, x, rows);
   }
   // forward, middle levels, then the top level
   for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
@@ -469,7 +487,7 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
         x.h_std = hs;
         x.counters = ln.counters;
       }
-      rc = launch_slice_on(c, vs[v], fused ? "ntt_dit_join" : "ntt_dit", k_ntt_dit, x, rows);
+      rc = launch_slice_on(c, vs[v], fused ? "ntt_dit_join" : "ntt_dit", Slice::dit, x, rows);
     }
   }
   if (rc != G3H_OK) return rc;
@@ -574,7 +592,7 @@ int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
   x.scale_tab = scale_load;
   x.kk = pl.kk[0];
   x.mode = (check ? SL_CHECK : 0u) | (scale_load ? SL_SCALE_TABLE : 0u);
-  int rc = launch_slice(c, "ntt_brev", k_ntt_brev, x, 1);
+  int rc = launch_slice(c, "ntt_brev", Slice::brev, x, 1);
   for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
     SliceArgs y = base_args(c, flags);
     const bool top = lvl == pl.levels - 1;
@@ -592,7 +610,7 @@ int ntt(g3h_ctx* c, fr_t* data, int inverse, int coset, uint32_t flags) {
         y.mode = SL_SCALE_CONST;
       }
     }
-    rc = launch_slice(c, "ntt_dit", k_ntt_dit, y, 1);
+    rc = launch_slice(c, "ntt_dit", Slice::dit, y, 1);
   }
   return rc;
 }
@@ -1280,13 +1298,12 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
     x.log_n = log_n;
     return x;
   };
-  auto geometry = [&](const SliceArgs& x, unsigned nvec, dim3* grid, dim3* block, size_t* smem) {
-    *grid = dim3((unsigned)(n >> x.kk), nvec);
-    *block = dim3(std::min(1u << (x.kk - 1u), kSliceThreads));
-    *smem = (size_t)32 << x.kk;
+  auto launch = [&](Slice which, const SliceArgs& x, unsigned nvec) {
+    uint32_t threads = 0;
+    void (*kern)(SliceArgs) = slice_kernel(which, x.kk, &threads);
+    const dim3 grid((unsigned)(n >> x.kk), nvec);
+    kern<<<grid, threads, (size_t)32 << x.kk, s>>>(x);
   };
-  dim3 grid, block;
-  size_t smem;
   SliceArgs x = args();
   for (int i = 0; i < 3; i++) {
     x.src[i] = in[i];
@@ -1295,16 +1312,14 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
   x.tw = tw_inv;
   x.kk = pl.kk[1];
   x.c0 = pl.c0[1];
-  geometry(x, 3, &grid, &block, &smem);
-  k_ntt_dif<<<grid, block, smem, s>>>(x);
+  launch(Slice::dif, x, 3);
   SliceArgs m = args();
   for (int i = 0; i < 3; i++) m.dst[i] = v[i];
   m.tw = tw_inv;
   m.tw2 = tw_fwd;
   m.scale_tab = shift;
   m.kk = pl.kk[0];
-  geometry(m, 3, &grid, &block, &smem);
-  k_ntt_mid<<<grid, block, smem, s>>>(m);
+  launch(Slice::mid, m, 3);
   SliceArgs t = args();
   for (int i = 0; i < 3; i++) t.src[i] = t.dst[i] = v[i];
   t.tw = tw_fwd;
@@ -1313,7 +1328,6 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
   t.mode = SL_JOIN;
   t.h_mont = hm;
   t.h_std = hs;
-  geometry(t, 1, &grid, &block, &smem);
-  k_ntt_dit<<<grid, block, smem, s>>>(t);
+  launch(Slice::dit, t, 1);
   return noalloc_launch_ok();
 }

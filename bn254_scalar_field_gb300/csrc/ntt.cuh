@@ -207,6 +207,145 @@ __device__ __forceinline__ void dit_pass(uint4* sm, uint32_t kk, const fr_const_
   __syncthreads();
 }
 
+// Two passes at once, on slice bits L and L + 1: a group of four elements e0 = base,
+// e1 = base + 2^L, e2 = base + 2^(L+1), e3 = e2 + 2^L (base with both bits clear), one
+// group per thread iteration, one barrier for the two passes. Groups run j-major (a warp
+// shares g_lo, hence every twiddle) when there are at least 32 groups per g_lo.
+struct Quad4 {
+  uint32_t e0, e1, e2, e3, glo;
+};
+
+__device__ __forceinline__ Quad4 quad_at(uint32_t g, uint32_t L, uint32_t kk) {
+  Quad4 q;
+  uint32_t glo, ghi;
+  const uint32_t hib = kk - L - 2u;  // log2 of the number of g_hi values
+  if (hib >= 5u) {
+    glo = g >> hib;
+    ghi = g & ((1u << hib) - 1u);
+  } else {
+    glo = g & ((1u << L) - 1u);
+    ghi = g >> L;
+  }
+  q.e0 = (ghi << (L + 2u)) | glo;
+  q.e1 = q.e0 + (1u << L);
+  q.e2 = q.e0 + (2u << L);
+  q.e3 = q.e2 + (1u << L);
+  q.glo = glo;
+  return q;
+}
+
+__device__ __forceinline__ uint32_t tw_index(uint32_t j, uint32_t b, uint32_t low, uint32_t c0,
+                                             uint32_t k) {
+  return (low + (j << c0)) << (k - 1u - c0 - b);
+}
+
+// Decimation in frequency on bits L + 1 (first) and L, then a barrier.
+__device__ __forceinline__ void dif_pass2(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
+                                          uint32_t L, uint32_t low, uint32_t c0, uint32_t k) {
+  const uint32_t size = 1u << kk;
+  for (uint32_t g = threadIdx.x; g < (size >> 2); g += blockDim.x) {
+    const Quad4 q = quad_at(g, L, kk);
+    fr_t x0 = sm_get(sm, size, q.e0), x1 = sm_get(sm, size, q.e1);
+    fr_t x2 = sm_get(sm, size, q.e2), x3 = sm_get(sm, size, q.e3);
+    const uint32_t ta = tw_index(q.glo, L + 1u, low, c0, k);
+    const uint32_t tb = tw_index(q.glo + (1u << L), L + 1u, low, c0, k);
+    const uint32_t tc = tw_index(q.glo, L, low, c0, k);
+    fr_t d02 = fr_sub(x0, x2), d13 = fr_sub(x1, x3);
+    x0 = fr_add(x0, x2);
+    x1 = fr_add(x1, x3);
+    if (ta != 0u) d02 = fr_mul_c(d02, fr_const_ldg(tw + ta));
+    d13 = fr_mul_c(d13, fr_const_ldg(tw + tb));  // tb != 0: its j has bit L set
+    // bit L: (x0, x1) and (d02, d13), both with twiddle tc
+    fr_t d01 = fr_sub(x0, x1), d23 = fr_sub(d02, d13);
+    sm_put(sm, size, q.e0, fr_add(x0, x1));
+    sm_put(sm, size, q.e2, fr_add(d02, d13));
+    if (tc != 0u) {
+      const fr_const_t wc = fr_const_ldg(tw + tc);
+      d01 = fr_mul_c(d01, wc);
+      d23 = fr_mul_c(d23, wc);
+    }
+    sm_put(sm, size, q.e1, d01);
+    sm_put(sm, size, q.e3, d23);
+  }
+  __syncthreads();
+}
+
+// Decimation in time on bits L (first) and L + 1, then a barrier.
+__device__ __forceinline__ void dit_pass2(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
+                                          uint32_t L, uint32_t low, uint32_t c0, uint32_t k) {
+  const uint32_t size = 1u << kk;
+  for (uint32_t g = threadIdx.x; g < (size >> 2); g += blockDim.x) {
+    const Quad4 q = quad_at(g, L, kk);
+    fr_t x0 = sm_get(sm, size, q.e0), x1 = sm_get(sm, size, q.e1);
+    fr_t x2 = sm_get(sm, size, q.e2), x3 = sm_get(sm, size, q.e3);
+    const uint32_t tc = tw_index(q.glo, L, low, c0, k);
+    const uint32_t ta = tw_index(q.glo, L + 1u, low, c0, k);
+    const uint32_t tb = tw_index(q.glo + (1u << L), L + 1u, low, c0, k);
+    // bit L: (x0, x1) and (x2, x3), twiddle tc on the upper elements
+    if (tc != 0u) {
+      const fr_const_t wc = fr_const_ldg(tw + tc);
+      x1 = fr_mul_c(x1, wc);
+      x3 = fr_mul_c(x3, wc);
+    }
+    fr_t y0 = fr_add(x0, x1), y1 = fr_sub(x0, x1);
+    fr_t y2 = fr_add(x2, x3), y3 = fr_sub(x2, x3);
+    // bit L + 1: (y0, y2) with ta, (y1, y3) with tb
+    if (ta != 0u) y2 = fr_mul_c(y2, fr_const_ldg(tw + ta));
+    y3 = fr_mul_c(y3, fr_const_ldg(tw + tb));
+    sm_put(sm, size, q.e0, fr_add(y0, y2));
+    sm_put(sm, size, q.e2, fr_sub(y0, y2));
+    sm_put(sm, size, q.e1, fr_add(y1, y3));
+    sm_put(sm, size, q.e3, fr_sub(y1, y3));
+  }
+  __syncthreads();
+}
+
+// All decimation-in-frequency passes of a slice (bits kk-1 .. 0), two at a time with R4.
+template <bool R4>
+__device__ __forceinline__ void dif_passes(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
+                                           uint32_t low, uint32_t c0, uint32_t k) {
+  int lb = (int)kk - 1;
+  if (R4)
+    for (; lb >= 1; lb -= 2) dif_pass2(sm, kk, tw, (uint32_t)lb - 1u, low, c0, k);
+  for (; lb >= 0; lb--) dif_pass(sm, kk, tw, (uint32_t)lb, low, c0, k);
+}
+
+// All decimation-in-time passes of a slice (bits 0 .. kk-1), two at a time with R4.
+template <bool R4>
+__device__ __forceinline__ void dit_passes(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
+                                           uint32_t low, uint32_t c0, uint32_t k) {
+  uint32_t lb = 0;
+  if (R4)
+    for (; lb + 1u < kk; lb += 2) dit_pass2(sm, kk, tw, lb, low, c0, k);
+  for (; lb < kk; lb++) dit_pass(sm, kk, tw, lb, low, c0, k);
+}
+
+// Two builds of each slice kernel. Configuration 1: radix-4 pass pairs, 128 threads,
+// five resident blocks per SM (up to 102 registers); configuration 0: radix-2 passes,
+// 256 threads, four blocks (64 registers). Measured on GB300: 1 is faster on slices of
+// 2^9 and 2^10 elements (2^18 H: 0.310 -> 0.295 ms; 2^20: 1.146 -> 1.071 ms), 0 on
+// smaller slices (2^12, 2^14: latency-bound, 0.069 vs 0.081 ms) and on the 2^11 slices of
+// 2^22 (4.97 vs 5.18 ms).
+template <int C>
+struct SliceCfg;
+template <>
+struct SliceCfg<0> {
+  static constexpr bool r4 = false;
+  static constexpr uint32_t threads = 256, min_blocks = 4;
+};
+template <>
+struct SliceCfg<1> {
+  static constexpr bool r4 = true;
+  static constexpr uint32_t threads = 128, min_blocks = 5;
+};
+#ifndef G3H_R4_MIN_BITS
+#define G3H_R4_MIN_BITS 9
+#endif
+#ifndef G3H_R4_MAX_BITS
+#define G3H_R4_MAX_BITS 10
+#endif
+constexpr uint32_t kRadix4MinSliceBits = G3H_R4_MIN_BITS, kRadix4MaxSliceBits = G3H_R4_MAX_BITS;
+
 // Block s of a strided slice kernel owns low = s mod 2^c0, high = s >> c0 and the
 // elements low + (m << c0) + (high << (c0 + kk)), m < 2^kk.
 __device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t kk) {
@@ -219,7 +358,8 @@ __device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t k
 // it writes). With SL_C_FROM_AB vector 2 is formed as a * b from vectors 0 and 1 at load.
 // Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), dynamic shared memory
 // 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif(const __grid_constant__ SliceArgs p) {
+template <int C>
+__global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dif(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
@@ -241,7 +381,7 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif
     }
   }
   __syncthreads();
-  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, kk, p.tw, (uint32_t)lb, low, c0, k);
+  dif_passes<SliceCfg<C>::r4>(sm, kk, p.tw, low, c0, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(dst + base + ((size_t)m << c0), sm_get(sm, size, m));
 }
@@ -253,7 +393,8 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dif
 // then the forward transform's decimation-in-time passes on bits 0 .. kk-1 (twiddles
 // p.tw2). In place. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
 // 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_mid(const __grid_constant__ SliceArgs p) {
+template <int C>
+__global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_mid(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
@@ -261,11 +402,11 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_mid
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_load(vec + base + m));
   __syncthreads();
-  for (int lb = (int)kk - 1; lb >= 0; lb--) dif_pass(sm, kk, p.tw, (uint32_t)lb, 0u, 0u, k);
+  dif_passes<SliceCfg<C>::r4>(sm, kk, p.tw, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_mul_c(sm_get(sm, size, m), fr_const_ldg(p.scale_tab + base + m)));
   __syncthreads();
-  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw2, lb, 0u, 0u, k);
+  dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw2, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(vec + base + m, sm_get(sm, size, m));
 }
@@ -284,7 +425,8 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_mid
 //   L2 and writes h, then resets the counter. No block ever waits for another.
 // Launch: grid (n >> kk, vectors; 1 with SL_JOIN), block min(2^(kk-1), 256), shared
 // 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dit(const __grid_constant__ SliceArgs p) {
+template <int C>
+__global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dit(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
@@ -299,7 +441,7 @@ __global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_dit
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
       sm_put(sm, size, m, fr_load(src + base + ((size_t)m << c0)));
     __syncthreads();
-    for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw, lb, low, c0, k);
+    dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw, low, c0, k);
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
       const size_t i = base + ((size_t)m << c0);
       const fr_t x = sm_get(sm, size, m);
