@@ -200,9 +200,21 @@ def cpu_baseline(A, B, w, budget_s=12.0, max_runs=20):
         oracle.compute_h(LOG_N, A, B, w)
         total += time.perf_counter() - t
         runs += 1
-    return {"value": runs / total, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d whole 2^18 H computations (%.1f s), C oracle, one thread" % (
-                runs, total)}
+    out = {"value": runs / total, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": "%d whole 2^18 H computations (%.1f s), C oracle, one thread" % (
+               runs, total)}
+    # the H multiexp's oracle (double-and-add per point) on a sample of the 2^18 bases,
+    # as points per second, beside the GPU's msm_2^18_per_s * 2^18
+    from bn254_scalar_field_gb300 import synth_g1
+
+    pts = synth_g1.points(512, seed=synth_g1.default_seed(LOG_N))
+    sc = synth_g1.scalars(512, seed=synth_g1.default_seed(LOG_N) + 1)
+    t = time.perf_counter()
+    oracle.g1_msm(pts, sc)
+    dt = time.perf_counter() - t
+    out["msm_points_per_s"] = 512 / dt
+    out["msm_sample"] = "512 of the 2^18 bases and scalars (%.2f s), C oracle, one thread" % dt
+    return out
 
 
 def run_reference(args, rank, world):
@@ -480,6 +492,7 @@ def h_msm(torch, dev, g3h, flush, steps=50):
     peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
     achieved = entries * MSM_OPS_PER_MADD / (acc_ms * 1e-3)
     return {"msm_2^18_ms": ms, "msm_2^18_per_s": 1e3 / ms,
+            "msm_2^18_points_per_s": n * 1e3 / ms,
             "msm_2^18_kernels_ms": {k2: v[1] / v[0] for k2, v in kt.items()},
             "msm_accumulate_t_imad_s": achieved / 1e12,
             "msm_accumulate_frac_of_derived_imad_peak": achieved / peak}

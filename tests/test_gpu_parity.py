@@ -120,8 +120,10 @@ def test_ntt_all_modes(log_n):
                 assert np.array_equal(got, want), (inverse, coset)
 
 
-@pytest.mark.parametrize("log_n", [20, 23])
+@pytest.mark.parametrize("log_n", [19, 20, 21, 23])
 def test_ntt_large_and_three_levels(log_n):
+    """2^19 and 2^20 run radix-4 pass pairs on 2^10 slices, 2^21 mixes 2^10 and 2^11
+    slices (radix-2 on the latter), 2^23 takes three levels."""
     n = 1 << log_n
     x = synth.uniform_fr(synth.SplitMix64(200 + log_n), n)
     with g3h.Context(log_n) as ctx:
@@ -255,6 +257,19 @@ def test_compute_h_abc_stress_2_22():
         ctx.compute_h_abc(a, b, c, hm, hs)
     assert np.array_equal(hm, want_m)
     assert np.array_equal(hs, want_s)
+
+
+@pytest.mark.parametrize("log_n", [19, 20])
+def test_compute_h_abc_radix4_slices(log_n):
+    """The quotient path on 2^10-element slices (radix-4 pass pairs in all three kernels)."""
+    n = 1 << log_n
+    rng = synth.SplitMix64(600 + log_n)
+    a, b, c = (synth.uniform_fr(rng, n) for _ in range(3))
+    want_m, want_s = oracle.compute_h_abc(log_n, a, b, c)
+    with g3h.Context(log_n) as ctx:
+        hm, hs = _zeros(n), _zeros(n)
+        ctx.compute_h_abc(a, b, c, hm, hs)
+    assert np.array_equal(hm, want_m) and np.array_equal(hs, want_s)
 
 
 def test_compute_h_abc_three_levels():
