@@ -570,7 +570,10 @@ def stress_2_22(torch, dev, g3h, synth):
     ctx.sync()
     ctx.close()
     peak = float(measured_peaks().get("hbm_gbs", 0.0)) or None
-    return {"ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,
+    ops = sum(algorithmic_ops(kn, k, 0, 0) for kn in ("ntt_dif", "ntt_mid", "ntt_dit", "join"))
+    imad_peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    return {"h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / imad_peak,
+            "ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,
             "h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
             "ntt_gelem_s_2^22_in_h": 6 * n / (h_ms * 1e-3) / 1e9,
             "mont_to_std_2^24_ms": m2s_ms, "mont_to_std_2^24_gb_s": m2s_gbs,

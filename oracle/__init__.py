@@ -63,6 +63,7 @@ def lib():
         L.orc_compute_h.restype = ctypes.c_int
         L.orc_compute_h_abc.argtypes = [U, P, P, P, P, P]
         L.orc_compute_h_abc.restype = ctypes.c_int
+        L.orc_poly_eval.argtypes = [S, P, P, P]
         L.orc_fq_mul.argtypes = [P, P, P]
         L.orc_fq_inv.argtypes = [P, P]
         for name, args in (("orc_g1_on_curve", [P]), ("orc_g1_add", [P, P, P]),
@@ -147,6 +148,15 @@ def domain(log_n):
     g = np.zeros(8, np.uint32)
     _check(lib().orc_domain(log_n, _p(w), _p(g)), "domain")
     return w, g
+
+
+def poly_eval(coeffs, z):
+    """sum_j coeffs[j] z^j (Montgomery in and out), one point."""
+    c = _fr(coeffs)
+    zz = _fr(z).reshape(8)
+    out = np.zeros(8, np.uint32)
+    lib().orc_poly_eval(c.shape[0], _p(c), _p(zz), _p(out))
+    return out
 
 
 def ntt(data, log_n, inverse=False, coset=False):

@@ -265,6 +265,17 @@ void orc_to_mont(const uint32_t* in, uint32_t* out, size_t n) {
 }
 
 /* omega_n and g in standard form (not Montgomery), for the pins. */
+/* sum_j coeffs[j] z^j over j < n by Horner's rule; coeffs and z Montgomery, out Montgomery
+ * (canonical). The definition of a forward transform's output e[i] = P(omega^i), or
+ * P(g omega^i) on the coset, one point at a time. */
+void orc_poly_eval(size_t n, const uint32_t* coeffs, const uint32_t* z, uint32_t* out) {
+  init();
+  const fe zz = load32(z);
+  fe acc = {{0, 0, 0, 0}};
+  for (size_t j = n; j-- > 0;) acc = fe_add(fe_mont_mul(acc, zz), load32(coeffs + 8 * j));
+  store32(out, acc);
+}
+
 int orc_domain(unsigned log_n, uint32_t* omega_std, uint32_t* g_std) {
   init();
   if (log_n > 27) return -1;

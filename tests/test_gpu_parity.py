@@ -134,6 +134,26 @@ def test_ntt_large_and_three_levels(log_n):
         assert np.array_equal(got, x)
 
 
+def test_ntt_largest_domain_sampled():
+    """The largest domain, 2^27 (4 GiB per vector): the forward coset transform's outputs
+    at sampled points against the oracle's Horner evaluation at g omega^i (the whole
+    oracle transform would take minutes), then the inverse brings back the input exactly."""
+    from oracle import fr_int as F
+
+    log_n = g3h.G3H_MAX_LOG_N
+    n = 1 << log_n
+    x = synth.uniform_fr(synth.SplitMix64(271), n)
+    omega, gen = (F.limbs_to_int(v) for v in oracle.domain(log_n))
+    with g3h.Context(log_n) as ctx:
+        got = x.copy()
+        ctx.ntt(got, coset=True)
+        for i in (0, 1, n // 2 + 12345, n - 1):
+            z = F.ints_to_array([F.to_mont(gen * pow(omega, i, F.R_MOD) % F.R_MOD)])
+            assert np.array_equal(got[i], oracle.poly_eval(x, z)), i
+        ctx.ntt(got, inverse=True, coset=True)
+        assert np.array_equal(got, x)
+
+
 # -------------------------------------------------------------------------- gather ----
 
 @pytest.mark.parametrize("log_n", [0, 1, 3, 7, 10, 12, 14])

@@ -158,6 +158,17 @@ def test_c_ntt_matches_definition(log_n, oracle_lib):
     assert got == [F.poly_eval(x, g * pow(omega, i, R) % R) for i in range(n)]
 
 
+def test_c_poly_eval_matches_python_horner(oracle_lib):
+    """The C single-point evaluation (used to sample outputs of transforms too large for
+    the whole oracle) against Python ints, at edge points and random ones."""
+    for n, seed in ((1, 1), (2, 2), (37, 3), (300, 4)):
+        x = _rand_vals(n, 700 + seed)
+        xm = F.ints_to_array([F.to_mont(v) for v in x])
+        for z in (0, 1, R - 1, _rand_vals(1, 800 + seed)[0]):
+            got = F.from_mont(F.limbs_to_int(oracle.poly_eval(xm, F.ints_to_array([F.to_mont(z)]))))
+            assert got == F.poly_eval(x, z)
+
+
 @pytest.mark.parametrize("log_n", [1, 4, 9])
 def test_ntt_special_inputs_and_round_trip(log_n, oracle_lib):
     n = 1 << log_n
