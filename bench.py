@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="skip the 2^22 secondary lines")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    p.add_argument("--msm-only", action="store_true",
+                   help="time only the 2^18 H multiexp over G1 (the extra line's "
+                        "measurement; for profiler captures of its kernels)")
     p.add_argument("--serialize", action="store_true",
                    help="headline pass too with the three vectors in one launch per phase "
                         "on one stream (for profiler captures of the kernels as the "
@@ -262,6 +265,16 @@ def main():
     from bn254_scalar_field_gb300 import build, g3h, synth
 
     torch.cuda.set_device(local)
+    if args.msm_only:
+        build.build()
+        dev = torch.device("cuda", local)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        r = h_msm(torch, dev, g3h, flush, steps=args.steps, warmup=args.warmup)
+        if rank == 0:
+            print(json.dumps({"metric": "G1 multiexp (the H MSM) at 2^18", "value": r["msm_2^18_per_s"],
+                              "unit": "MSM/s", "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": True, "data": "synthetic", "extra": r}))
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -451,7 +464,7 @@ def batched(torch, dev, ctx, w, n, flush, count=8, reps=20):
 MSM_OPS_PER_MADD = (8 + 2) * OPS_PER_MM  # madd-2008-s: 8 multiplies + 2 squarings
 
 
-def h_msm(torch, dev, g3h, flush, steps=50):
+def h_msm(torch, dev, g3h, flush, steps=50, warmup=3):
     """The H multiexp at 2^18 (sum of h_i P_i over G1, h uniform in [0, r), bases sampled
     on the curve): device buffers, bases prepared once (untimed), L2 flushed between
     steps. Roofline of the bucket accumulation: one mixed addition per nonzero window
@@ -467,7 +480,7 @@ def h_msm(torch, dev, g3h, flush, steps=50):
     sd = torch.from_numpy(sc.view(np.int32)).to(dev)
     res = torch.zeros(24, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(3):
+    for _ in range(max(warmup, 1)):
         ctx.msm(sd, res)
     evs = []
     for i in range(steps):
@@ -486,12 +499,41 @@ def h_msm(torch, dev, g3h, flush, steps=50):
     kt = ctx.timing_read()
     ctx.timing_enable(False)
     ctx.sync()
+    # a witness multiexp on the same bases: the 2^18 proving-key witness (99 % of wires 0
+    # or 1) in standard form, made on the device
+    from bn254_scalar_field_gb300 import synth
+
+    _, _, w = synth.problem(k)
+    wd = torch.from_numpy(w.view(np.int32)).to(dev)
+    ws = torch.empty_like(wd)
+    ctx.mont_to_std(wd, ws)
+    for _ in range(3):
+        ctx.msm(ws, res)
+    wevs = []
+    for i in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.fill_(i & 0xFF)
+        e0.record(stream)
+        ctx.msm(ws, res)
+        e1.record(stream)
+        wevs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    wit_ms = statistics.median(a.elapsed_time(b) for a, b in wevs)
+    ctx.timing_enable(True)
+    for i in range(10):
+        flush.fill_(i & 0xFF)
+        ctx.msm(ws, res)
+    wkt = ctx.timing_read()
+    ctx.timing_enable(False)
+    ctx.sync()
     ctx.close()
     entries = 16 * n  # nonzero digits: all but about 2^-16 of them
     acc_ms = kt["msm_accumulate"][1] / kt["msm_accumulate"][0]
     peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
     achieved = entries * MSM_OPS_PER_MADD / (acc_ms * 1e-3)
     return {"msm_2^18_ms": ms, "msm_2^18_per_s": 1e3 / ms,
+            "witness_msm_2^18_ms": wit_ms,
+            "witness_msm_2^18_kernels_ms": {k2: v[1] / v[0] for k2, v in wkt.items()},
             "msm_2^18_points_per_s": n * 1e3 / ms,
             "msm_2^18_kernels_ms": {k2: v[1] / v[0] for k2, v in kt.items()},
             "msm_accumulate_t_imad_s": achieved / 1e12,

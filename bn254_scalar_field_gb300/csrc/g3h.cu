@@ -172,7 +172,7 @@ struct g3h_ctx {
   g1_xyzz_t* d_msm_buckets = nullptr;   // per bucket
   g1_xyzz_t* d_msm_spill = nullptr;     // head | tail parts, (n + 1) each
   g1_xyzz_t* d_msm_groups = nullptr;    // U | V, kMsmPairs each
-  g1_xyzz_t* d_msm_parts = nullptr;     // chunk sums (kMsmSumParts * kMsmChunks) | parts
+  g1_xyzz_t* d_msm_parts = nullptr;     // chunk sums | parts, ones' sum | ones' block sums
   fq_t* d_msm_result = nullptr;         // Jacobian X, Y, Z
   bool timing = false;
   std::vector<TimedLaunch> launches;
@@ -1016,7 +1016,26 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
   if (cudaMemsetAsync(c->d_msm_counts, 0, kMsmBuckets * sizeof(uint32_t), st) != cudaSuccess)
     return G3H_E_CUDA;
   const unsigned grid = (unsigned)std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
-  int rc = run(c, "msm_count", [&] {
+  g1_xyzz_t* parts = c->d_msm_parts + kMsmSumParts * kMsmChunks;
+  g1_xyzz_t* ones = parts + kMsmSumParts + 1;
+  const unsigned ones_grid = (unsigned)c->sm_count * 2;
+  // the ones' sum runs on a second stream beside the bucket path, joined before the end
+  Lane& ln = c->own;
+  cudaStream_t os = ln.aux[0];
+  int rc = cudaEventRecord(ln.ev_fork, st) == cudaSuccess &&
+                   cudaStreamWaitEvent(os, ln.ev_fork, 0) == cudaSuccess
+               ? G3H_OK
+               : G3H_E_CUDA;
+  if (rc == G3H_OK)
+    rc = run_on(c, os, "msm_ones", [&] {
+      k_msm_ones<<<ones_grid, 256, 0, os>>>(s, count, c->d_msm_table, ones);
+    });
+  if (rc == G3H_OK)
+    rc = run_on(c, os, "msm_ones_sum", [&] {
+      k_msm_ones_sum<<<1, 256, 0, os>>>(ones, ones_grid, parts);
+    });
+  if (rc == G3H_OK && cudaEventRecord(ln.ev_end[0], os) != cudaSuccess) rc = G3H_E_CUDA;
+  if (rc == G3H_OK) rc = run(c, "msm_count", [&] {
     k_msm_count<<<grid, 256, 0, st>>>(s, count, c->d_msm_counts, check, c->d_err);
   });
   if (rc == G3H_OK)
@@ -1027,10 +1046,12 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
     rc = run(c, "msm_scatter", [&] {
       k_msm_scatter<<<grid, 256, 0, st>>>(s, count, c->d_msm_cursor, c->d_msm_entries);
     });
-  // slices of equal length, about one per resident thread of the accumulation kernel
+  // threads for slices of equal length, about one per resident thread of the accumulation
+  // kernel for the most entries there can be; the kernels size the slices to the entries
+  // present (at least kMsmMinSlice each), so n_slices <= count <= the spill slots
   const uint64_t max_entries = (uint64_t)count * kMsmWindows;
   const uint32_t slice = (uint32_t)std::max<uint64_t>(
-      16, (max_entries + c->msm_slots - 1) / std::max<uint32_t>(c->msm_slots, 1));
+      kMsmMinSlice, (max_entries + c->msm_slots - 1) / std::max<uint32_t>(c->msm_slots, 1));
   const uint32_t n_slices = (uint32_t)((max_entries + slice - 1) / slice);
   g1_xyzz_t* head = c->d_msm_spill;
   g1_xyzz_t* tail = c->d_msm_spill + c->msm_n + 1;
@@ -1038,12 +1059,12 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
     rc = run(c, "msm_accumulate", [&] {
       k_msm_accumulate<<<blocks_for(n_slices, 256), 256, 0, st>>>(
           c->d_msm_entries, c->d_msm_offsets, c->d_msm_table, c->d_msm_buckets, head, tail,
-          slice, n_slices);
+          n_slices);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_merge", [&] {
       k_msm_merge<<<kMsmBuckets / 128, 128, 0, st>>>(c->d_msm_offsets, c->d_msm_buckets, head,
-                                                      tail, slice);
+                                                      tail, n_slices);
     });
   g1_xyzz_t* U = c->d_msm_groups;
   g1_xyzz_t* V = c->d_msm_groups + kMsmPairs;
@@ -1056,11 +1077,11 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
       k_msm_part_chunks<<<dim3(kMsmChunks, kMsmSumParts), 256, 256 * sizeof(g1_xyzz_t), st>>>(
           U, V, c->d_msm_parts);
     });
-  g1_xyzz_t* parts = c->d_msm_parts + kMsmSumParts * kMsmChunks;
   if (rc == G3H_OK)
     rc = run(c, "msm_parts", [&] {
       k_msm_parts<<<kMsmSumParts, 32, 0, st>>>(c->d_msm_parts, parts);
     });
+  if (rc == G3H_OK && cudaStreamWaitEvent(st, ln.ev_end[0], 0) != cudaSuccess) rc = G3H_E_CUDA;
   if (rc == G3H_OK)
     rc = run(c, "msm_final", [&] { k_msm_final<<<1, 32, 0, st>>>(parts, out); });
   return rc;
@@ -1082,7 +1103,10 @@ int g3h_msm_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_buckets, kMsmBuckets);
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_spill, 2 * (n + 1));
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_groups, 2 * kMsmPairs);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_parts, kMsmSumParts * (kMsmChunks + 1));
+  // chunk sums | the parts and the ones' sum | the ones' block sums
+  if (rc == G3H_OK)
+    rc = dalloc(&c->d_msm_parts,
+                kMsmSumParts * kMsmChunks + kMsmSumParts + 1 + (size_t)c->sm_count * 2);
   if (rc == G3H_OK) rc = dalloc(&c->d_msm_result, 3);
   int per_sm = 0;
   if (rc == G3H_OK &&

@@ -10,6 +10,8 @@
 //   B_j = sum over (i, w) with |d_{i,w}| = j of sign(d_{i,w}) 2^(16 w) P_i,
 // one set of 2^15 buckets for all windows: no per-window bucket sums and no doubling
 // chain between windows. Steps:
+//   0. ones: the bases whose scalar is exactly 1 are summed apart (a tree per block, then
+//      one block), so they do not pile into one bucket;
 //   1. count: per-bucket entry counts (32-bit atomics on counters, never on points);
 //   2. scan: exclusive prefix sum of the counts (bucket offsets);
 //   3. scatter: each (i, w) entry, as (16 i + w) << 1 | sign, into its bucket's run
@@ -44,6 +46,13 @@ __device__ __forceinline__ int msm_digit(const uint32_t* s, uint32_t w, uint32_t
   }
   carry = 0u;
   return (int)v;
+}
+
+// Scalars equal to 1 (half of a typical witness) would all be one entry of bucket 1 and
+// make one bucket's run as long as the rest together (MSM_CU, "scalars 0 and 1 never reach
+// a bucket"); they are summed apart, by k_msm_ones. Scalars 0 give no entries anyway.
+__device__ __forceinline__ bool msm_is_one(const uint32_t* s) {
+  return s[0] == 1u && (s[1] | s[2] | s[3] | s[4] | s[5] | s[6] | s[7]) == 0u;
 }
 
 __device__ __forceinline__ void msm_load_scalar(const fr_t* scalars, uint32_t i, uint32_t* s,
@@ -91,6 +100,7 @@ __global__ void __launch_bounds__(256) k_msm_count(const fr_t* scalars, uint32_t
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     uint32_t s[8];
     msm_load_scalar(scalars, i, s, check, err);
+    if (msm_is_one(s)) continue;  // summed by k_msm_ones
     uint32_t carry = 0;
 #pragma unroll
     for (uint32_t w = 0; w < kMsmWindows; w++) {
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(256) k_msm_scatter(const fr_t* scalars, uint32
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     uint32_t s[8];
     msm_load_scalar(scalars, i, s, 0u, nullptr);
+    if (msm_is_one(s)) continue;
     uint32_t carry = 0;
 #pragma unroll
     for (uint32_t w = 0; w < kMsmWindows; w++) {
@@ -165,17 +176,27 @@ __global__ void __launch_bounds__(256) k_msm_scatter(const fr_t* scalars, uint32
   }
 }
 
+// Slice length: the entries present (offsets[kMsmBuckets], known only here) spread over the
+// n_slices threads launched for the most there can be, at least kMsmMinSlice per thread (a
+// run cut into more slices costs its bucket more additions at the merge). The merge
+// computes the same length.
+constexpr uint32_t kMsmMinSlice = 16;
+
+__device__ __forceinline__ uint32_t msm_slice_len(uint32_t total, uint32_t n_slices) {
+  return max(kMsmMinSlice, (total + n_slices - 1u) / n_slices);
+}
+
 // Step 4: slice k = entries [k L, min(k L + L, total)). Launch: ceil(n_slices / 256)
 // blocks of 256; slices past the total exit.
 __global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
                                                         const uint32_t* offsets,
                                                         const g1_aff_t* table,
                                                         g1_xyzz_t* buckets, g1_xyzz_t* head,
-                                                        g1_xyzz_t* tail, uint32_t slice,
-                                                        uint32_t n_slices) {
+                                                        g1_xyzz_t* tail, uint32_t n_slices) {
   const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= n_slices) return;
   const uint32_t total = offsets[kMsmBuckets];
+  const uint32_t slice = msm_slice_len(total, n_slices);
   const uint32_t lo = k * slice;
   if (lo >= total) return;
   const uint32_t hi = min(lo + slice, total);
@@ -227,9 +248,10 @@ __device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<F
 // Launch: kMsmBuckets / 128 blocks of 128.
 __global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, g1_xyzz_t* buckets,
                                                    const g1_xyzz_t* head, const g1_xyzz_t* tail,
-                                                   uint32_t slice) {
+                                                   uint32_t n_slices) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= kMsmBuckets) return;
+  const uint32_t slice = msm_slice_len(offsets[kMsmBuckets], n_slices);
   const uint32_t s = offsets[j], e = offsets[j + 1];
   if (s == e) {
     buckets[j] = xyzz_infinity();
@@ -329,11 +351,52 @@ __global__ void __launch_bounds__(32) k_msm_parts(const g1_xyzz_t* partial, g1_x
   }
 }
 
-// Step 9: Q = the sum of the 15 parts (shuffles), written in Jacobian coordinates,
-// canonical Montgomery, infinity as (0, 0, 0). Launch: one block of 32.
+// The sum of the bases whose scalar is 1, beside the bucket path: each thread adds its
+// share (grid-stride, mixed additions of the bases, which are the window-0 table entries),
+// then a tree per block leaves one point per block in partial[blockIdx.x].
+// Launch: any grid of 256 threads.
+__global__ void __launch_bounds__(256) k_msm_ones(const fr_t* scalars, uint32_t n,
+                                                  const g1_aff_t* table, g1_xyzz_t* partial) {
+  __shared__ g1_xyzz_t sm[256];
+  const uint32_t stride = gridDim.x * blockDim.x, tid = threadIdx.x;
+  g1_xyzz_t acc = xyzz_infinity();
+  for (uint32_t i = blockIdx.x * blockDim.x + tid; i < n; i += stride) {
+    const fr_t x = fr_load(scalars + i);
+    if (!msm_is_one(x.v)) continue;
+    const g1_aff_t p = table[(size_t)i * kMsmWindows];
+    if (!aff_is_inf(p)) acc = xyzz_madd(acc, p);
+  }
+  sm[tid] = acc;
+  __syncthreads();
+  for (uint32_t d = 128; d > 0; d >>= 1) {
+    if (tid < d) sm[tid] = xyzz_add_nl(sm[tid], sm[tid + d]);
+    __syncthreads();
+  }
+  if (tid == 0) partial[blockIdx.x] = sm[0];
+}
+
+// The block sums of k_msm_ones (count of them) into one point, parts[kMsmSumParts].
+// Launch: one block of 256.
+__global__ void __launch_bounds__(256) k_msm_ones_sum(const g1_xyzz_t* partial, uint32_t count,
+                                                      g1_xyzz_t* parts) {
+  __shared__ g1_xyzz_t sm[256];
+  const uint32_t tid = threadIdx.x;
+  g1_xyzz_t acc = xyzz_infinity();
+  for (uint32_t i = tid; i < count; i += blockDim.x) acc = xyzz_add_nl(acc, partial[i]);
+  sm[tid] = acc;
+  __syncthreads();
+  for (uint32_t d = 128; d > 0; d >>= 1) {
+    if (tid < d) sm[tid] = xyzz_add_nl(sm[tid], sm[tid + d]);
+    __syncthreads();
+  }
+  if (tid == 0) parts[kMsmSumParts] = sm[0];
+}
+
+// Step 9: Q = the sum of the 15 parts and the ones' sum (shuffles), written in Jacobian
+// coordinates, canonical Montgomery, infinity as (0, 0, 0). Launch: one block of 32.
 __global__ void __launch_bounds__(32) k_msm_final(const g1_xyzz_t* parts, fq_t* out) {
   const uint32_t lane = threadIdx.x;
-  g1_xyzz_t acc = lane < kMsmSumParts ? parts[lane] : xyzz_infinity();
+  g1_xyzz_t acc = lane <= kMsmSumParts ? parts[lane] : xyzz_infinity();
   for (uint32_t d = 8; d > 0; d >>= 1) {
     const g1_xyzz_t o = xyzz_shfl_down(acc, d);
     if (lane < d) acc = xyzz_add_nl(acc, o);

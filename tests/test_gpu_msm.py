@@ -7,7 +7,7 @@ oracle's own arithmetic and compared limb for limb with the oracle's sum of s_i 
 Cases: ragged sizes (1 .. 4099 bases, fewer scalars than bases, none), host and device
 buffers, scalars at the digit boundaries (2^15, 2^15 + 1, 2^16 - 1 in a window: the
 signed-digit carry), 0, 1, r - 1, one scalar for every base (all entries in a few
-buckets: the slices' load balance), equal bases with equal scalars (the doubling case of
+buckets: the slices' load balance), witness scalars (mostly 0 and 1), equal bases with equal scalars (the doubling case of
 the mixed addition), P and -P (cancellation), bases at infinity, the chain from
 g3h_compute_h's h_std, the full 2^18 workload, and the input checks.
 """
@@ -164,6 +164,29 @@ def test_msm_on_h_std():
         got = _affine(res.cpu().numpy().view(np.uint32))
     _, want_hs = oracle.compute_h(log_n, A, B, w)
     assert np.array_equal(got, oracle.g1_msm(pts, want_hs))
+
+
+@pytest.mark.parametrize("log_n", [12, 14])
+def test_witness_msm_over_g1(log_n):
+    """A witness multiexp (MSM_CU stages 5, 6, 8 over G1): the witness of the proving-key
+    workload (90 / 95 % of wires 0 or 1) brought to standard form on the device
+    (g3h_mont_to_std), then summed against bases; zeros add no entry, ones one entry each
+    in the first bucket, which the slices spread over many threads."""
+    import torch
+
+    _, _, w = synth.problem(log_n)
+    n = w.shape[0]
+    pts = synth_g1.points(n, seed=900 + log_n)
+    with g3h.Context(0) as ctx:
+        wd = _dev(w)
+        ws = torch.empty_like(wd)
+        ctx.mont_to_std(wd, ws)
+        ctx.msm_prepare(_dev(pts))
+        res = _dev(np.zeros(24, np.uint32))
+        ctx.msm(ws, res)
+        ctx.sync()
+        got = _affine(res.cpu().numpy().view(np.uint32))
+    assert np.array_equal(got, _oracle_msm(pts, oracle.from_mont(w)))
 
 
 def test_msm_full_2p18():
