@@ -68,7 +68,10 @@ def lib():
         L.orc_fq_inv.argtypes = [P, P]
         for name, args in (("orc_g1_on_curve", [P]), ("orc_g1_add", [P, P, P]),
                            ("orc_g1_mul", [P, P, P]), ("orc_g1_msm", [S, P, P, P]),
-                           ("orc_g1_jacobian_to_affine", [P, P])):
+                           ("orc_g1_jacobian_to_affine", [P, P]),
+                           ("orc_g2_on_curve", [P]), ("orc_g2_add", [P, P, P]),
+                           ("orc_g2_mul", [P, P, P]), ("orc_g2_msm", [S, P, P, P]),
+                           ("orc_g2_jacobian_to_affine", [P, P])):
             getattr(L, name).argtypes = args
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -269,4 +272,48 @@ def g1_jacobian_to_affine(jac):
     j = np.ascontiguousarray(jac, dtype=np.uint32).reshape(24)
     out = np.zeros(16, np.uint32)
     lib().orc_g1_jacobian_to_affine(_p(j), _p(out))
+    return out
+
+
+# ------------------------------------------------------------------------- G2 ----
+
+def _pts2(a):
+    return np.ascontiguousarray(a, dtype=np.uint32).reshape(-1, 32)
+
+
+def g2_on_curve(points):
+    pts = _pts2(points)
+    return np.array([bool(lib().orc_g2_on_curve(_p(pts[i]))) for i in range(pts.shape[0])])
+
+
+def g2_add(p, q):
+    p, q = _pts2(p), _pts2(q)
+    out = np.empty_like(p)
+    for i in range(p.shape[0]):
+        lib().orc_g2_add(_p(p[i]), _p(q[i]), _p(out[i]))
+    return out
+
+
+def g2_mul(points, scalars):
+    pts, k = _pts2(points), _fr(scalars)
+    out = np.empty_like(pts)
+    for i in range(pts.shape[0]):
+        lib().orc_g2_mul(_p(pts[i]), _p(k[i]), _p(out[i]))
+    return out
+
+
+def g2_msm(points, scalars):
+    """sum_i scalars[i] * points[i] over the twist, one affine point, shape (32,)."""
+    pts, k = _pts2(points), _fr(scalars)
+    if pts.shape[0] != k.shape[0]:
+        raise ValueError("points and scalars differ in length")
+    out = np.zeros(32, np.uint32)
+    lib().orc_g2_msm(pts.shape[0], _p(pts), _p(k), _p(out))
+    return out
+
+
+def g2_jacobian_to_affine(jac):
+    j = np.ascontiguousarray(jac, dtype=np.uint32).reshape(48)
+    out = np.zeros(32, np.uint32)
+    lib().orc_g2_jacobian_to_affine(_p(j), _p(out))
     return out

@@ -311,3 +311,166 @@ int orc_g1_jacobian_to_affine(const uint32_t* p, uint32_t* out) {
   P.Z = load_fq(p + 16);
   return store_affine(out, P);
 }
+
+/* ================================================================= G2 over F_q2 ====
+ *
+ * The same definition over the twist E': y^2 = x^3 + b2 over F_q2 = F_q[u]/(u^2 + 1),
+ * b2 = 3 / (9 + u) (EIP-197), the witness multiexp of the B query (MSM_CU stage 7). The
+ * point formulas are the Jacobian ones above with F_q2 arithmetic; an affine point is
+ * x.c0, x.c1, y.c0, y.c1 (32 limbs), a Jacobian one X, Y, Z (48 limbs), each coordinate
+ * c0 + c1 u in Montgomery form over F_q. */
+
+typedef struct {
+  fq c0, c1;
+} fq2;
+
+static fq2 f2_add(fq2 a, fq2 b) { fq2 r = {fq_add(a.c0, b.c0), fq_add(a.c1, b.c1)}; return r; }
+static fq2 f2_sub(fq2 a, fq2 b) { fq2 r = {fq_sub(a.c0, b.c0), fq_sub(a.c1, b.c1)}; return r; }
+
+/* (a0 + a1 u)(b0 + b1 u) = (a0 b0 - a1 b1) + (a0 b1 + a1 b0) u, by the schoolbook formula */
+static fq2 f2_mul(fq2 a, fq2 b) {
+  fq2 r;
+  r.c0 = fq_sub(fq_mul(a.c0, b.c0), fq_mul(a.c1, b.c1));
+  r.c1 = fq_add(fq_mul(a.c0, b.c1), fq_mul(a.c1, b.c0));
+  return r;
+}
+
+static int f2_is_zero(fq2 a) { return fq_is_zero(a.c0) && fq_is_zero(a.c1); }
+static int f2_eq(fq2 a, fq2 b) { return fq_eq(a.c0, b.c0) && fq_eq(a.c1, b.c1); }
+
+/* 1 / (a0 + a1 u) = (a0 - a1 u) / (a0^2 + a1^2) */
+static fq2 f2_inv(fq2 a) {
+  fq n = fq_inv(fq_add(fq_mul(a.c0, a.c0), fq_mul(a.c1, a.c1)));
+  fq zero = {{0, 0, 0, 0}};
+  fq2 r = {fq_mul(a.c0, n), fq_mul(fq_sub(zero, a.c1), n)};
+  return r;
+}
+
+static fq2 load_fq2(const uint32_t* p) { fq2 a = {load_fq(p), load_fq(p + 8)}; return a; }
+static void store_fq2(uint32_t* p, fq2 a) { store_fq(p, a.c0); store_fq(p + 8, a.c1); }
+
+static fq2 twist_b(void) {
+  fq2 three = {small(3), {{0, 0, 0, 0}}};
+  fq2 nine_u = {small(9), ONE};
+  return f2_mul(three, f2_inv(nine_u));
+}
+
+typedef struct {
+  fq2 X, Y, Z; /* Z = 0: the point at infinity */
+} jac2;
+
+static jac2 jac2_infinity(void) {
+  jac2 r;
+  memset(&r, 0, sizeof r);
+  r.X.c0 = ONE;
+  r.Y.c0 = ONE;
+  return r;
+}
+
+/* the tangent formula of jac_double, over F_q2 */
+static jac2 jac2_double(jac2 P) {
+  if (f2_is_zero(P.Z) || f2_is_zero(P.Y)) return jac2_infinity();
+  fq2 XX = f2_mul(P.X, P.X), YY = f2_mul(P.Y, P.Y);
+  fq2 M = f2_add(f2_add(XX, XX), XX);
+  fq2 XYY = f2_mul(P.X, YY);
+  fq2 S = f2_add(XYY, XYY);
+  S = f2_add(S, S);
+  fq2 Y4 = f2_mul(YY, YY);
+  fq2 Y4x8 = f2_add(Y4, Y4);
+  Y4x8 = f2_add(Y4x8, Y4x8);
+  Y4x8 = f2_add(Y4x8, Y4x8);
+  fq2 YZ = f2_mul(P.Y, P.Z);
+  jac2 R;
+  R.X = f2_sub(f2_mul(M, M), f2_add(S, S));
+  R.Y = f2_sub(f2_mul(M, f2_sub(S, R.X)), Y4x8);
+  R.Z = f2_add(YZ, YZ);
+  return R;
+}
+
+/* the chord formula of jac_add, over F_q2 */
+static jac2 jac2_add(jac2 P, jac2 Qp) {
+  if (f2_is_zero(P.Z)) return Qp;
+  if (f2_is_zero(Qp.Z)) return P;
+  fq2 Z1Z1 = f2_mul(P.Z, P.Z), Z2Z2 = f2_mul(Qp.Z, Qp.Z);
+  fq2 U1 = f2_mul(P.X, Z2Z2), U2 = f2_mul(Qp.X, Z1Z1);
+  fq2 S1 = f2_mul(P.Y, f2_mul(Qp.Z, Z2Z2)), S2 = f2_mul(Qp.Y, f2_mul(P.Z, Z1Z1));
+  if (f2_eq(U1, U2)) {
+    if (f2_eq(S1, S2)) return jac2_double(P);
+    return jac2_infinity();
+  }
+  fq2 H = f2_sub(U2, U1), r = f2_sub(S2, S1);
+  fq2 HH = f2_mul(H, H), HHH = f2_mul(H, HH);
+  fq2 V = f2_mul(U1, HH);
+  jac2 R;
+  R.X = f2_sub(f2_sub(f2_mul(r, r), HHH), f2_add(V, V));
+  R.Y = f2_sub(f2_mul(r, f2_sub(V, R.X)), f2_mul(S1, HHH));
+  R.Z = f2_mul(H, f2_mul(P.Z, Qp.Z));
+  return R;
+}
+
+static jac2 jac2_mul(jac2 P, const uint32_t* k) {
+  jac2 acc = jac2_infinity();
+  for (int i = 255; i >= 0; i--) {
+    acc = jac2_double(acc);
+    if ((k[i / 32] >> (i % 32)) & 1) acc = jac2_add(acc, P);
+  }
+  return acc;
+}
+
+static jac2 load_affine2(const uint32_t* p) {
+  jac2 P;
+  P.X = load_fq2(p);
+  P.Y = load_fq2(p + 16);
+  if (f2_is_zero(P.X) && f2_is_zero(P.Y)) return jac2_infinity();
+  memset(&P.Z, 0, sizeof P.Z);
+  P.Z.c0 = ONE;
+  return P;
+}
+
+static int store_affine2(uint32_t* out, jac2 P) {
+  if (f2_is_zero(P.Z)) {
+    memset(out, 0, 32 * sizeof(uint32_t));
+    return 1;
+  }
+  fq2 zi = f2_inv(P.Z);
+  fq2 zi2 = f2_mul(zi, zi);
+  store_fq2(out, f2_mul(P.X, zi2));
+  store_fq2(out + 16, f2_mul(P.Y, f2_mul(zi2, zi)));
+  return 0;
+}
+
+int orc_g2_on_curve(const uint32_t* p) {
+  init();
+  fq2 x = load_fq2(p), y = load_fq2(p + 16);
+  if (f2_is_zero(x) && f2_is_zero(y)) return 1;
+  if (fq_geq(&x.c0, &Q) || fq_geq(&x.c1, &Q) || fq_geq(&y.c0, &Q) || fq_geq(&y.c1, &Q))
+    return 0;
+  return f2_eq(f2_mul(y, y), f2_add(f2_mul(f2_mul(x, x), x), twist_b()));
+}
+
+int orc_g2_add(const uint32_t* p, const uint32_t* q, uint32_t* out) {
+  init();
+  return store_affine2(out, jac2_add(load_affine2(p), load_affine2(q)));
+}
+
+int orc_g2_mul(const uint32_t* p, const uint32_t* k, uint32_t* out) {
+  init();
+  return store_affine2(out, jac2_mul(load_affine2(p), k));
+}
+
+int orc_g2_msm(size_t n, const uint32_t* bases, const uint32_t* scalars, uint32_t* out) {
+  init();
+  jac2 acc = jac2_infinity();
+  for (size_t i = 0; i < n; i++)
+    acc = jac2_add(acc, jac2_mul(load_affine2(bases + 32 * i), scalars + 8 * i));
+  return store_affine2(out, acc);
+}
+
+int orc_g2_jacobian_to_affine(const uint32_t* p, uint32_t* out) {
+  init();
+  jac2 P;
+  P.X = load_fq2(p);
+  P.Y = load_fq2(p + 16);
+  P.Z = load_fq2(p + 32);
+  return store_affine2(out, P);
+}
