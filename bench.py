@@ -270,6 +270,7 @@ def main():
         dev = torch.device("cuda", local)
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
         r = h_msm(torch, dev, g3h, flush, steps=args.steps, warmup=args.warmup)
+        r.update(g2_msm(torch, dev, g3h, flush, steps=args.steps))
         if rank == 0:
             print(json.dumps({"metric": "G1 multiexp (the H MSM) at 2^18", "value": r["msm_2^18_per_s"],
                               "unit": "MSM/s", "steps": args.steps, "warmup": args.warmup,
@@ -404,6 +405,7 @@ def main():
     extra.update(batched(torch, dev, ctx, w, n, flush))
     if not args.no_extra and rank == 0:
         extra.update(h_msm(torch, dev, g3h, flush))
+        extra.update(g2_msm(torch, dev, g3h, flush))
         extra.update(other_domains(torch, dev, g3h, synth, flush))
         extra.update(stress_2_22(torch, dev, g3h, synth))
     ctx.close()
@@ -538,6 +540,50 @@ def h_msm(torch, dev, g3h, flush, steps=50, warmup=3):
             "msm_2^18_kernels_ms": {k2: v[1] / v[0] for k2, v in kt.items()},
             "msm_accumulate_t_imad_s": achieved / 1e12,
             "msm_accumulate_frac_of_derived_imad_peak": achieved / peak}
+
+
+MSM_G2_OPS_PER_MADD = (8 * 3 + 2 * 2) * OPS_PER_MM  # F_q2: 3 F_q multiplies, 2 per square
+
+
+def g2_msm(torch, dev, g3h, flush, k=16, steps=20):
+    """The multiexp over the twist (G2, the B query's) on 2^16 sampled twist points with
+    uniform scalars: device buffers, bases prepared once, L2 flushed between steps."""
+    from bn254_scalar_field_gb300 import synth_g1, synth_g2
+
+    n = 1 << k
+    pts = synth_g2.points(n, seed=synth_g2.default_seed(k))
+    sc = synth_g1.scalars(n, seed=synth_g2.default_seed(k) + 1)
+    ctx = g3h.Context(0, device=dev.index)
+    ctx.msm_g2_prepare(torch.from_numpy(pts.view(np.int32)).to(dev))
+    sd = torch.from_numpy(sc.view(np.int32)).to(dev)
+    res = torch.zeros(48, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        ctx.msm_g2(sd, res)
+    evs = []
+    for i in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.fill_(i & 0xFF)
+        e0.record(stream)
+        ctx.msm_g2(sd, res)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    ctx.timing_enable(True)
+    for i in range(5):
+        flush.fill_(i & 0xFF)
+        ctx.msm_g2(sd, res)
+    kt = ctx.timing_read()
+    ctx.timing_enable(False)
+    ctx.sync()
+    ctx.close()
+    acc_ms = kt["msm_accumulate"][1] / kt["msm_accumulate"][0]
+    peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    achieved = 16 * n * MSM_G2_OPS_PER_MADD / (acc_ms * 1e-3)
+    return {"msm_g2_2^%d_ms" % k: ms,
+            "msm_g2_2^%d_kernels_ms" % k: {k2: v[1] / v[0] for k2, v in kt.items()},
+            "msm_g2_accumulate_frac_of_derived_imad_peak": achieved / peak}
 
 
 def other_domains(torch, dev, g3h, synth, flush, steps=200):

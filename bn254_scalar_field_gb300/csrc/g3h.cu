@@ -125,6 +125,22 @@ void free_lane_streams(Lane& l) {
     if (e) cudaEventDestroy(e);
 }
 
+// The buffers of one group's multiexp (bytes as raw device memory, typed at use).
+struct MsmState {
+  uint32_t n = 0;                    // bases prepared
+  uint32_t slots = 0;                // resident threads of the accumulation kernel
+  void* table = nullptr;             // 16 affine points per base: 2^(16 w) P_i
+  uint32_t* entries = nullptr;       // 16 per base
+  uint32_t* counts = nullptr;        // per bucket
+  uint32_t* offsets = nullptr;       // per bucket + 1
+  uint32_t* cursor = nullptr;        // per bucket
+  void* buckets = nullptr;           // per bucket
+  void* spill = nullptr;             // head | tail parts, (n + 1) each
+  void* groups = nullptr;            // U | V, kMsmPairs each
+  void* parts = nullptr;             // chunk sums | the parts and the ones' sum | ones' block sums
+  void* result = nullptr;            // Jacobian X, Y, Z
+};
+
 struct g3h_ctx {
   int device = 0;
   int sm_count = 1;
@@ -161,19 +177,8 @@ struct g3h_ctx {
   std::vector<Graph> graphs;
   std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
   cudaEvent_t batch_start = nullptr;
-  // multi-scalar multiplication over G1 (g3h_msm_prepare / g3h_msm)
-  uint32_t msm_n = 0;                   // bases prepared
-  uint32_t msm_slots = 0;               // resident threads of k_msm_accumulate
-  g1_aff_t* d_msm_table = nullptr;      // 16 per base: 2^(16 w) P_i
-  uint32_t* d_msm_entries = nullptr;    // 16 per base
-  uint32_t* d_msm_counts = nullptr;     // per bucket
-  uint32_t* d_msm_offsets = nullptr;    // per bucket + 1
-  uint32_t* d_msm_cursor = nullptr;     // per bucket
-  g1_xyzz_t* d_msm_buckets = nullptr;   // per bucket
-  g1_xyzz_t* d_msm_spill = nullptr;     // head | tail parts, (n + 1) each
-  g1_xyzz_t* d_msm_groups = nullptr;    // U | V, kMsmPairs each
-  g1_xyzz_t* d_msm_parts = nullptr;     // chunk sums | parts, ones' sum | ones' block sums
-  fq_t* d_msm_result = nullptr;         // Jacobian X, Y, Z
+  // multiexps over G1 and G2 (g3h_msm_prepare / g3h_msm and the _g2 pair)
+  MsmState msm1, msm2;
   bool timing = false;
   std::vector<TimedLaunch> launches;
   std::vector<cudaEvent_t> event_pool;
@@ -188,21 +193,17 @@ int dalloc(T** p, size_t count) {
   return cudaMalloc((void**)p, count * sizeof(T)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
 }
 
-void msm_free(g3h_ctx* c) {
-  void* bufs[] = {c->d_msm_table,   c->d_msm_entries, c->d_msm_counts, c->d_msm_offsets,
-                  c->d_msm_cursor,  c->d_msm_buckets, c->d_msm_spill,  c->d_msm_groups,
-                  c->d_msm_parts,   c->d_msm_result};
+void msm_free(MsmState& m) {
+  void* bufs[] = {m.table, m.entries, m.counts, m.offsets, m.cursor,
+                  m.buckets, m.spill, m.groups, m.parts, m.result};
   for (void* b : bufs)
     if (b) cudaFree(b);
-  c->d_msm_table = nullptr;
-  c->d_msm_entries = c->d_msm_counts = c->d_msm_offsets = c->d_msm_cursor = nullptr;
-  c->d_msm_buckets = c->d_msm_spill = c->d_msm_groups = c->d_msm_parts = nullptr;
-  c->d_msm_result = nullptr;
-  c->msm_n = 0;
+  m = MsmState();
 }
 
 void release(g3h_ctx* c) {
-  msm_free(c);
+  msm_free(c->msm1);
+  msm_free(c->msm2);
   void* bufs[] = {c->d_rpa,      c->d_cola,     c->d_rpb,      c->d_colb,        c->d_vala,
                   c->d_valb,     c->d_consts,   c->d_tw_fwd,   c->d_tw_inv,      c->d_shift_br,
                   c->d_coset_fwd, c->d_coset_inv, c->d_abc,    c->d_stage,       c->d_err,
@@ -1011,13 +1012,26 @@ int g3h_mont_to_std(g3h_ctx* c, const uint32_t* in, uint32_t* out, size_t count,
 // ---------------------------------------------------------------------------------------
 // Multi-scalar multiplication over G1.
 
-int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t check) {
+}  // extern "C"
+
+namespace {
+
+template <class G>
+int msm_launches(g3h_ctx* c, MsmState& m, const fr_t* s, uint32_t count, typename G::F* out,
+                 uint32_t check) {
+  using Pt = typename G::Pt;
+  using Aff = typename G::Aff;
+  constexpr uint32_t T = G::kTree;
+  constexpr uint32_t chunks = msm_chunks<G>();
   cudaStream_t st = c->stream;
-  if (cudaMemsetAsync(c->d_msm_counts, 0, kMsmBuckets * sizeof(uint32_t), st) != cudaSuccess)
+  if (cudaMemsetAsync(m.counts, 0, kMsmBuckets * sizeof(uint32_t), st) != cudaSuccess)
     return G3H_E_CUDA;
   const unsigned grid = (unsigned)std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
-  g1_xyzz_t* parts = c->d_msm_parts + kMsmSumParts * kMsmChunks;
-  g1_xyzz_t* ones = parts + kMsmSumParts + 1;
+  const Aff* table = (const Aff*)m.table;
+  Pt* buckets = (Pt*)m.buckets;
+  Pt* chunk_sums = (Pt*)m.parts;
+  Pt* parts = chunk_sums + kMsmSumParts * chunks;
+  Pt* ones = parts + kMsmSumParts + 1;
   const unsigned ones_grid = (unsigned)c->sm_count * 2;
   // the ones' sum runs on a second stream beside the bucket path, joined before the end
   Lane& ln = c->own;
@@ -1028,130 +1042,135 @@ int msm_launches(g3h_ctx* c, const fr_t* s, uint32_t count, fq_t* out, uint32_t 
                : G3H_E_CUDA;
   if (rc == G3H_OK)
     rc = run_on(c, os, "msm_ones", [&] {
-      k_msm_ones<<<ones_grid, 256, 0, os>>>(s, count, c->d_msm_table, ones);
+      k_msm_ones<G><<<ones_grid, T, 0, os>>>(s, count, table, ones);
     });
   if (rc == G3H_OK)
     rc = run_on(c, os, "msm_ones_sum", [&] {
-      k_msm_ones_sum<<<1, 256, 0, os>>>(ones, ones_grid, parts);
+      k_msm_ones_sum<G><<<1, T, 0, os>>>(ones, ones_grid, parts);
     });
   if (rc == G3H_OK && cudaEventRecord(ln.ev_end[0], os) != cudaSuccess) rc = G3H_E_CUDA;
   if (rc == G3H_OK) rc = run(c, "msm_count", [&] {
-    k_msm_count<<<grid, 256, 0, st>>>(s, count, c->d_msm_counts, check, c->d_err);
+    k_msm_count<<<grid, 256, 0, st>>>(s, count, m.counts, check, c->d_err);
   });
   if (rc == G3H_OK)
     rc = run(c, "msm_scan", [&] {
-      k_msm_scan<<<1, 1024, 0, st>>>(c->d_msm_counts, c->d_msm_offsets, c->d_msm_cursor);
+      k_msm_scan<<<1, 1024, 0, st>>>(m.counts, m.offsets, m.cursor);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_scatter", [&] {
-      k_msm_scatter<<<grid, 256, 0, st>>>(s, count, c->d_msm_cursor, c->d_msm_entries);
+      k_msm_scatter<<<grid, 256, 0, st>>>(s, count, m.cursor, m.entries);
     });
   // threads for slices of equal length, about one per resident thread of the accumulation
   // kernel for the most entries there can be; the kernels size the slices to the entries
   // present (at least kMsmMinSlice each), so n_slices <= count <= the spill slots
   const uint64_t max_entries = (uint64_t)count * kMsmWindows;
   const uint32_t slice = (uint32_t)std::max<uint64_t>(
-      kMsmMinSlice, (max_entries + c->msm_slots - 1) / std::max<uint32_t>(c->msm_slots, 1));
+      kMsmMinSlice, (max_entries + m.slots - 1) / std::max<uint32_t>(m.slots, 1));
   const uint32_t n_slices = (uint32_t)((max_entries + slice - 1) / slice);
-  g1_xyzz_t* head = c->d_msm_spill;
-  g1_xyzz_t* tail = c->d_msm_spill + c->msm_n + 1;
+  Pt* head = (Pt*)m.spill;
+  Pt* tail = head + m.n + 1;
   if (rc == G3H_OK)
     rc = run(c, "msm_accumulate", [&] {
-      k_msm_accumulate<<<blocks_for(n_slices, 256), 256, 0, st>>>(
-          c->d_msm_entries, c->d_msm_offsets, c->d_msm_table, c->d_msm_buckets, head, tail,
-          n_slices);
+      k_msm_accumulate<G><<<blocks_for(n_slices, T), T, 0, st>>>(
+          m.entries, m.offsets, table, buckets, head, tail, n_slices);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_merge", [&] {
-      k_msm_merge<<<kMsmBuckets / 128, 128, 0, st>>>(c->d_msm_offsets, c->d_msm_buckets, head,
-                                                      tail, n_slices);
+      k_msm_merge<G><<<kMsmBuckets / 128, 128, 0, st>>>(m.offsets, buckets, head, tail, n_slices);
     });
-  g1_xyzz_t* U = c->d_msm_groups;
-  g1_xyzz_t* V = c->d_msm_groups + kMsmPairs;
+  Pt* U = (Pt*)m.groups;
+  Pt* V = U + kMsmPairs;
   if (rc == G3H_OK)
     rc = run(c, "msm_pairs", [&] {
-      k_msm_pairs<<<kMsmPairs / 128, 128, 0, st>>>(c->d_msm_buckets, U, V);
+      k_msm_pairs<G><<<kMsmPairs / 128, 128, 0, st>>>(buckets, U, V);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_part_chunks", [&] {
-      k_msm_part_chunks<<<dim3(kMsmChunks, kMsmSumParts), 256, 256 * sizeof(g1_xyzz_t), st>>>(
-          U, V, c->d_msm_parts);
+      k_msm_part_chunks<G><<<dim3(chunks, kMsmSumParts), T, 0, st>>>(U, V, chunk_sums);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_parts", [&] {
-      k_msm_parts<<<kMsmSumParts, 32, 0, st>>>(c->d_msm_parts, parts);
+      k_msm_parts<G><<<kMsmSumParts, 32, 0, st>>>(chunk_sums, parts);
     });
   if (rc == G3H_OK && cudaStreamWaitEvent(st, ln.ev_end[0], 0) != cudaSuccess) rc = G3H_E_CUDA;
   if (rc == G3H_OK)
-    rc = run(c, "msm_final", [&] { k_msm_final<<<1, 32, 0, st>>>(parts, out); });
+    rc = run(c, "msm_final", [&] { k_msm_final<G><<<1, 32, 0, st>>>(parts, out); });
   return rc;
 }
 
-int g3h_msm_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_t flags) {
+template <class G>
+int msm_prepare(g3h_ctx* c, MsmState& m, const uint32_t* bases, uint32_t n_bases,
+                uint32_t flags) {
+  using Pt = typename G::Pt;
+  using Aff = typename G::Aff;
   if (!c || (!bases && n_bases)) return G3H_E_INVAL;
   if (n_bases > (1u << G3H_MSM_MAX_LOG)) return G3H_E_RANGE;
   DeviceGuard guard(c->device);
   if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
-  msm_free(c);
+  msm_free(m);
   if (n_bases == 0) return G3H_OK;
   const size_t n = n_bases;
-  int rc = dalloc(&c->d_msm_table, n * kMsmWindows);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_entries, n * kMsmWindows);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_counts, kMsmBuckets);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_offsets, kMsmBuckets + 1);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_cursor, kMsmBuckets);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_buckets, kMsmBuckets);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_spill, 2 * (n + 1));
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_groups, 2 * kMsmPairs);
-  // chunk sums | the parts and the ones' sum | the ones' block sums
+  auto alloc = [](void** p, size_t bytes) {
+    return cudaMalloc(p, std::max<size_t>(bytes, 1)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+  };
+  int rc = alloc(&m.table, n * kMsmWindows * sizeof(Aff));
+  if (rc == G3H_OK) rc = dalloc(&m.entries, n * kMsmWindows);
+  if (rc == G3H_OK) rc = dalloc(&m.counts, kMsmBuckets);
+  if (rc == G3H_OK) rc = dalloc(&m.offsets, kMsmBuckets + 1);
+  if (rc == G3H_OK) rc = dalloc(&m.cursor, kMsmBuckets);
+  if (rc == G3H_OK) rc = alloc(&m.buckets, kMsmBuckets * sizeof(Pt));
+  if (rc == G3H_OK) rc = alloc(&m.spill, 2 * (n + 1) * sizeof(Pt));
+  if (rc == G3H_OK) rc = alloc(&m.groups, 2 * kMsmPairs * sizeof(Pt));
   if (rc == G3H_OK)
-    rc = dalloc(&c->d_msm_parts,
-                kMsmSumParts * kMsmChunks + kMsmSumParts + 1 + (size_t)c->sm_count * 2);
-  if (rc == G3H_OK) rc = dalloc(&c->d_msm_result, 3);
+    rc = alloc(&m.parts, (kMsmSumParts * msm_chunks<G>() + kMsmSumParts + 1 +
+                          (size_t)c->sm_count * 2) * sizeof(Pt));
+  if (rc == G3H_OK) rc = alloc(&m.result, 3 * sizeof(typename G::F));
   int per_sm = 0;
   if (rc == G3H_OK &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_msm_accumulate, 256, 0) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_msm_accumulate<G>, G::kTree, 0) !=
           cudaSuccess)
     rc = G3H_E_CUDA;
-  c->msm_slots = (uint32_t)std::max(per_sm, 1) * 256u * (uint32_t)c->sm_count;
-  g1_aff_t* src = (g1_aff_t*)bases;
-  g1_aff_t* tmp = nullptr;
+  m.slots = (uint32_t)std::max(per_sm, 1) * G::kTree * (uint32_t)c->sm_count;
+  const Aff* src = (const Aff*)bases;
+  void* tmp = nullptr;
   if (rc == G3H_OK && !(flags & G3H_DEVICE_PTRS)) {
-    rc = dalloc(&tmp, n);
-    if (rc == G3H_OK) rc = h2d(c, tmp, bases, n * sizeof(g1_aff_t));
-    src = tmp;
+    rc = alloc(&tmp, n * sizeof(Aff));
+    if (rc == G3H_OK) rc = h2d(c, tmp, bases, n * sizeof(Aff));
+    src = (const Aff*)tmp;
   }
   if (rc == G3H_OK)
     rc = run(c, "msm_precompute", [&] {
-      k_msm_precompute<<<blocks_for(n, 128), 128, 0, c->stream>>>(src, n_bases, c->d_msm_table,
-                                                                  c->d_err);
+      k_msm_precompute<G><<<blocks_for(n, 128), 128, 0, c->stream>>>(src, n_bases, (Aff*)m.table,
+                                                                     c->d_err);
     });
   const int rc2 = finish(c);
   if (tmp) cudaFree(tmp);
   if (rc == G3H_OK) rc = rc2;
   if (rc != G3H_OK) {
-    msm_free(c);
+    msm_free(m);
     return rc;
   }
-  c->msm_n = n_bases;
+  m.n = n_bases;
   return G3H_OK;
 }
 
-int g3h_msm(g3h_ctx* c, const uint32_t* scalars, uint32_t count, uint32_t* result,
+template <class G>
+int msm_run(g3h_ctx* c, MsmState& m, const uint32_t* scalars, uint32_t count, uint32_t* result,
             uint32_t flags) {
+  using F = typename G::F;
   if (!c || !result || (!scalars && count)) return G3H_E_INVAL;
-  if (count > c->msm_n) return G3H_E_RANGE;
+  if (count > m.n) return G3H_E_RANGE;
   DeviceGuard guard(c->device);
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   if (count == 0) {  // the empty sum: infinity
     if (dev)
-      return cudaMemsetAsync(result, 0, 3 * sizeof(fq_t), c->stream) == cudaSuccess ? G3H_OK
-                                                                                   : G3H_E_CUDA;
-    std::memset(result, 0, 3 * sizeof(fq_t));
+      return cudaMemsetAsync(result, 0, 3 * sizeof(F), c->stream) == cudaSuccess ? G3H_OK
+                                                                                : G3H_E_CUDA;
+    std::memset(result, 0, 3 * sizeof(F));
     return G3H_OK;
   }
-  fq_t* out = dev ? (fq_t*)result : c->d_msm_result;
+  F* out = dev ? (F*)result : (F*)m.result;
   const fr_t* s = (const fr_t*)scalars;
   int rc = G3H_OK;
   if (!dev) {
@@ -1159,11 +1178,37 @@ int g3h_msm(g3h_ctx* c, const uint32_t* scalars, uint32_t count, uint32_t* resul
     if (rc == G3H_OK) rc = h2d(c, c->d_stage, scalars, (size_t)count * sizeof(fr_t));
     s = c->d_stage;
   }
-  if (rc == G3H_OK) rc = msm_launches(c, s, count, out, check);
+  if (rc == G3H_OK) rc = msm_launches<G>(c, m, s, count, out, check);
   if (dev) return rc;
-  if (rc == G3H_OK) rc = d2h(c, result, out, 3 * sizeof(fq_t));
+  if (rc == G3H_OK) rc = d2h(c, result, out, 3 * sizeof(F));
   const int rc2 = finish(c);
   return rc != G3H_OK ? rc : rc2;
+}
+
+}  // namespace
+
+extern "C" {
+
+int g3h_msm_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_t flags) {
+  if (!c) return G3H_E_INVAL;
+  return msm_prepare<G1>(c, c->msm1, bases, n_bases, flags);
+}
+
+int g3h_msm(g3h_ctx* c, const uint32_t* scalars, uint32_t count, uint32_t* result,
+            uint32_t flags) {
+  if (!c) return G3H_E_INVAL;
+  return msm_run<G1>(c, c->msm1, scalars, count, result, flags);
+}
+
+int g3h_msm_g2_prepare(g3h_ctx* c, const uint32_t* bases, uint32_t n_bases, uint32_t flags) {
+  if (!c) return G3H_E_INVAL;
+  return msm_prepare<G2>(c, c->msm2, bases, n_bases, flags);
+}
+
+int g3h_msm_g2(g3h_ctx* c, const uint32_t* scalars, uint32_t count, uint32_t* result,
+               uint32_t flags) {
+  if (!c) return G3H_E_INVAL;
+  return msm_run<G2>(c, c->msm2, scalars, count, result, flags);
 }
 
 int g3h_sync(g3h_ctx* c) {
@@ -1188,7 +1233,7 @@ const char* g3h_strerror(int code) {
     case G3H_E_RANGE: return "value out of range (log_n, CSR row pointers or column index)";
     case G3H_E_NOMEM: return "out of memory";
     case G3H_E_CUDA: return "CUDA runtime error";
-    case G3H_E_POINT: return "a base point is not on the curve y^2 = x^3 + 3";
+    case G3H_E_POINT: return "a multiexp base point is not on its curve";
     default: return "unknown error";
   }
 }

@@ -29,12 +29,89 @@
 #pragma once
 #include "fr.cuh"
 #include "g1.cuh"
+#include "g2.cuh"
 
 namespace g3h {
 
 constexpr uint32_t kMsmWindows = 16;          // windows of 16 bits
 constexpr uint32_t kMsmBuckets = 1u << 15;    // digit magnitudes 1 .. 2^15
 constexpr uint32_t kMsmErrPoint = 2u;  // error word bit: a base is not on the curve
+
+// The bucket sum's point operations (see the kernels below) call out-of-line copies built
+// on one out-of-line multiply, so that the code their few warps loop over stays in the
+// instruction cache.
+using FqTail = FqCall;
+__device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) {
+  return xyzz_add_t<FqTail>(a, b);
+}
+__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<FqTail>(a); }
+__device__ __noinline__ g2_xyzz_t g2_add_nl(g2_xyzz_t a, g2_xyzz_t b) {
+  return g2_add_t<FqCall>(a, b);
+}
+__device__ __noinline__ g2_xyzz_t g2_dbl_nl(g2_xyzz_t a) { return g2_dbl_t<FqCall>(a); }
+
+template <class P>
+__device__ __forceinline__ P pt_shfl_down(const P& p, uint32_t d) {
+  constexpr int words = sizeof(P) / 4;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&p);
+  P o;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int w = 0; w < words; w++) dst[w] = __shfl_down_sync(0xffffffffu, src[w], d);
+  return o;
+}
+
+// The group of a multiexp: its point types and operations. G1: points of E over F_q, the
+// bucket additions inlined (many warps keep the multiply pipe busy). G2: points of the
+// twist over F_q2, every multiply out of line (an inlined F_q2 addition would be some
+// 90 KB of code), trees of 128 threads (points of 256 bytes in shared memory).
+struct G1 {
+  using Aff = g1_aff_t;
+  using Pt = g1_xyzz_t;
+  using F = fq_t;
+  static constexpr uint32_t kTree = 256;
+  static __device__ __forceinline__ Pt inf() { return xyzz_infinity(); }
+  static __device__ __forceinline__ bool aff_inf(const Aff& a) { return aff_is_inf(a); }
+  static __device__ __forceinline__ Aff neg(const Aff& a) { return aff_neg(a); }
+  static __device__ __forceinline__ Pt madd(const Pt& acc, const Aff& a) { return xyzz_madd(acc, a); }
+  static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return xyzz_add(a, b); }
+  static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return xyzz_add_nl(a, b); }
+  static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return xyzz_dbl_nl(a); }
+  static __device__ __forceinline__ void jacobian(const Pt& p, F* out) {
+    xyzz_to_jacobian_t<FqTail>(p, out[0], out[1], out[2]);
+  }
+  static __device__ __forceinline__ bool canonical(const Aff& a) {
+    return fq_is_canonical(a.x) && fq_is_canonical(a.y);
+  }
+  static __device__ __forceinline__ bool on_curve(const Aff& a) { return aff_on_curve(a); }
+  static __device__ __forceinline__ Aff zero_aff() { return {fq_zero(), fq_zero()}; }
+  static __device__ __forceinline__ Pt from_aff(const Aff& a) { return xyzz_from_aff(a); }
+  static __device__ __forceinline__ Pt dbl(const Pt& p) { return xyzz_dbl(p); }
+  static __device__ __forceinline__ Aff to_aff(const Pt& p) { return xyzz_to_aff(p); }
+};
+
+struct G2 {
+  using Aff = g2_aff_t;
+  using Pt = g2_xyzz_t;
+  using F = fq2_t;
+  static constexpr uint32_t kTree = 128;
+  static __device__ __forceinline__ Pt inf() { return g2_infinity(); }
+  static __device__ __forceinline__ bool aff_inf(const Aff& a) { return g2_aff_is_inf(a); }
+  static __device__ __forceinline__ Aff neg(const Aff& a) { return g2_aff_neg(a); }
+  static __device__ __forceinline__ Pt madd(const Pt& acc, const Aff& a) { return g2_madd_t<FqCall>(acc, a); }
+  static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
+  static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
+  static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return g2_dbl_nl(a); }
+  static __device__ __forceinline__ void jacobian(const Pt& p, F* out) { g2_to_jacobian_t<FqCall>(p, out); }
+  static __device__ __forceinline__ bool canonical(const Aff& a) {
+    return fq2_is_canonical(a.x) && fq2_is_canonical(a.y);
+  }
+  static __device__ __forceinline__ bool on_curve(const Aff& a) { return g2_aff_on_curve(a); }
+  static __device__ __forceinline__ Aff zero_aff() { return {fq2_zero(), fq2_zero()}; }
+  static __device__ __forceinline__ Pt from_aff(const Aff& a) { return g2_from_aff(a); }
+  static __device__ __forceinline__ Pt dbl(const Pt& p) { return g2_dbl_t<FqCall>(p); }
+  static __device__ __forceinline__ Aff to_aff(const Pt& p) { return g2_to_aff(p); }
+};
 
 // Signed 16-bit digit w of the scalar s (eight 32-bit limbs), given the carry out of
 // window w - 1; updates the carry.
@@ -66,29 +143,29 @@ __device__ __forceinline__ void msm_load_scalar(const fr_t* scalars, uint32_t i,
 // Prepare: table[16 i + w] = 2^(16 w) P_i, affine, canonical; a base at infinity (0, 0)
 // gives 16 points at infinity. Checks that each base is canonical and on the curve.
 // Launch: ceil(n / 128) blocks of 128.
-__global__ void __launch_bounds__(128) k_msm_precompute(const g1_aff_t* bases, uint32_t n,
-                                                        g1_aff_t* table, uint32_t* err) {
+template <class G>
+__global__ void __launch_bounds__(128) k_msm_precompute(const typename G::Aff* bases, uint32_t n,
+                                                        typename G::Aff* table, uint32_t* err) {
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  g1_aff_t b = bases[i];
-  g1_aff_t* out = table + (size_t)i * kMsmWindows;
-  if (aff_is_inf(b)) {
+  typename G::Aff b = bases[i];
+  typename G::Aff* out = table + (size_t)i * kMsmWindows;
+  if (G::aff_inf(b)) {
     for (uint32_t w = 0; w < kMsmWindows; w++) out[w] = b;
     return;
   }
-  if (!fq_is_canonical(b.x) || !fq_is_canonical(b.y)) {
+  if (!G::canonical(b)) {
     atomicOr(err, 1u);
-    b.x = fq_zero();
-    b.y = fq_zero();
+    b = G::zero_aff();
     for (uint32_t w = 0; w < kMsmWindows; w++) out[w] = b;
     return;
   }
-  if (!aff_on_curve(b)) atomicOr(err, kMsmErrPoint);
+  if (!G::on_curve(b)) atomicOr(err, kMsmErrPoint);
   out[0] = b;
-  g1_xyzz_t p = xyzz_from_aff(b);
+  typename G::Pt p = G::from_aff(b);
   for (uint32_t w = 1; w < kMsmWindows; w++) {
-    for (int d = 0; d < 16; d++) p = xyzz_dbl(p);
-    out[w] = xyzz_to_aff(p);
+    for (int d = 0; d < 16; d++) p = G::dbl(p);
+    out[w] = G::to_aff(p);
   }
 }
 
@@ -186,13 +263,13 @@ __device__ __forceinline__ uint32_t msm_slice_len(uint32_t total, uint32_t n_sli
   return max(kMsmMinSlice, (total + n_slices - 1u) / n_slices);
 }
 
-// Step 4: slice k = entries [k L, min(k L + L, total)). Launch: ceil(n_slices / 256)
-// blocks of 256; slices past the total exit.
-__global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
-                                                        const uint32_t* offsets,
-                                                        const g1_aff_t* table,
-                                                        g1_xyzz_t* buckets, g1_xyzz_t* head,
-                                                        g1_xyzz_t* tail, uint32_t n_slices) {
+// Step 4: slice k = entries [k L, min(k L + L, total)). Launch: ceil(n_slices / T)
+// blocks of T (256 for G1, 128 for G2); slices past the total exit.
+template <class G>
+__global__ void __launch_bounds__(G::kTree) k_msm_accumulate(
+    const uint32_t* entries, const uint32_t* offsets, const typename G::Aff* table,
+    typename G::Pt* buckets, typename G::Pt* head, typename G::Pt* tail, uint32_t n_slices) {
+  using Pt = typename G::Pt;
   const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= n_slices) return;
   const uint32_t total = offsets[kMsmBuckets];
@@ -208,7 +285,7 @@ __global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
   }
   uint32_t b = a;
   uint32_t run_end = offsets[b + 1];
-  g1_xyzz_t acc = xyzz_infinity();
+  Pt acc = G::inf();
   auto emit = [&]() {
     if (offsets[b] < lo) head[k] = acc;
     else if (run_end > hi) tail[k] = acc;
@@ -217,136 +294,123 @@ __global__ void __launch_bounds__(256) k_msm_accumulate(const uint32_t* entries,
   for (uint32_t i = lo; i < hi; i++) {
     if (i == run_end) {
       emit();
-      acc = xyzz_infinity();
+      acc = G::inf();
       do {
         b++;
         run_end = offsets[b + 1];
       } while (run_end <= i);
     }
     const uint32_t e = entries[i];
-    g1_aff_t p = table[e >> 1];
-    if (aff_is_inf(p)) continue;
-    if (e & 1u) p = aff_neg(p);
-    acc = xyzz_madd(acc, p);
+    typename G::Aff p = table[e >> 1];
+    if (G::aff_inf(p)) continue;
+    if (e & 1u) p = G::neg(p);
+    acc = G::madd(acc, p);
   }
   emit();
 }
 
-// The bucket sum below is a chain of dependent point operations on few threads: its time
-// is their latency, not throughput, and with few warps per SM nothing hides instruction
-// fetch. Its kernels call these out-of-line copies, which call one out-of-line multiply,
-// so that the code each thread loops over stays small and resident in the instruction
-// cache.
-using FqTail = FqCall;
-__device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) {
-  return xyzz_add_t<FqTail>(a, b);
-}
-__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<FqTail>(a); }
-
 // Step 5: one thread per bucket. A bucket with no entries is set to infinity; a run cut by
 // slice boundaries is the tail part of its first slice plus the head parts of the rest.
 // Launch: kMsmBuckets / 128 blocks of 128.
-__global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, g1_xyzz_t* buckets,
-                                                   const g1_xyzz_t* head, const g1_xyzz_t* tail,
-                                                   uint32_t n_slices) {
+template <class G>
+__global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, typename G::Pt* buckets,
+                                                   const typename G::Pt* head,
+                                                   const typename G::Pt* tail, uint32_t n_slices) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= kMsmBuckets) return;
   const uint32_t slice = msm_slice_len(offsets[kMsmBuckets], n_slices);
   const uint32_t s = offsets[j], e = offsets[j + 1];
   if (s == e) {
-    buckets[j] = xyzz_infinity();
+    buckets[j] = G::inf();
     return;
   }
   const uint32_t k_lo = s / slice, k_hi = (e - 1u) / slice;
   if (k_lo == k_hi) return;
-  g1_xyzz_t acc = tail[k_lo];
-  for (uint32_t k = k_lo + 1; k <= k_hi; k++) acc = xyzz_add(acc, head[k]);
+  typename G::Pt acc = tail[k_lo];
+  for (uint32_t k = k_lo + 1; k <= k_hi; k++) acc = G::add(acc, head[k]);
   buckets[j] = acc;
 }
 
 // The weighted sum Q = sum_j (j + 1) B_j. With pairs t = (B_2t, B_2t+1), digits 2t + 1 and
 // 2t + 2: U_t = B_2t + B_2t+1 and V_t = U_t + B_2t+1 = B_2t + 2 B_2t+1, so
 //   Q = sum_t (V_t + 2t U_t) = sum_t V_t + sum_{b < 14} 2^(b+1) sum_{t : bit b of t} U_t.
-// Part p < 14 is the sum over U_t with bit p of t set; part 14 is the sum of V.
+// Part p < 14 is the sum over U_t with bit p of t set; part 14 is the sum of V. The point
+// operations of steps 6-9 are a chain of some thirty dependent ones on few warps: their
+// time is latency, and they use the out-of-line copies (add_nl, dbl_nl).
 constexpr uint32_t kMsmPairs = kMsmBuckets / 2;          // 16384 = 2^14
 constexpr uint32_t kMsmPairBits = 14;
 constexpr uint32_t kMsmSumParts = kMsmPairBits + 1;      // 15
-constexpr uint32_t kMsmChunk = 512;                      // items per block in step 7
-constexpr uint32_t kMsmChunks = kMsmPairs / kMsmChunk;   // 32 (16 for the bit parts)
+
+// items per block in step 7 (two per thread) and chunks of the V part (the bit parts have
+// half as many)
+template <class G>
+__host__ __device__ constexpr uint32_t msm_chunk() { return 2 * G::kTree; }
+template <class G>
+__host__ __device__ constexpr uint32_t msm_chunks() { return kMsmPairs / msm_chunk<G>(); }
 
 // Step 6: U_t, V_t. Launch: kMsmPairs / 128 blocks of 128.
-__global__ void __launch_bounds__(128) k_msm_pairs(const g1_xyzz_t* buckets, g1_xyzz_t* U,
-                                                   g1_xyzz_t* V) {
+template <class G>
+__global__ void __launch_bounds__(128) k_msm_pairs(const typename G::Pt* buckets,
+                                                   typename G::Pt* U, typename G::Pt* V) {
   const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= kMsmPairs) return;
-  const g1_xyzz_t hi = buckets[2 * t + 1];
-  const g1_xyzz_t u = xyzz_add_nl(buckets[2 * t], hi);
+  const typename G::Pt hi = buckets[2 * t + 1];
+  const typename G::Pt u = G::add_nl(buckets[2 * t], hi);
   U[t] = u;
-  V[t] = xyzz_add_nl(u, hi);
+  V[t] = G::add_nl(u, hi);
 }
 
-// Step 7: partial sums of the parts, chunk c of part p = blockIdx (c, p): 512 items, two per
-// thread, then a tree in shared memory. The bit parts have 8192 items (16 chunks): item i
-// is t with bit p set, i.e. bit p inserted into i. Launch: grid (kMsmChunks, kMsmSumParts),
-// 256 threads, 256 * 128 bytes of dynamic shared memory.
-__global__ void __launch_bounds__(256) k_msm_part_chunks(const g1_xyzz_t* U, const g1_xyzz_t* V,
-                                                         g1_xyzz_t* partial) {
-  extern __shared__ g1_xyzz_t sm_pts[];
+// Step 7: partial sums of the parts, chunk c of part p = blockIdx (c, p): 2 T items, two per
+// thread, then a tree in shared memory. The bit parts have 8192 items: item i is t with
+// bit p set, i.e. bit p inserted into i. Launch: grid (msm_chunks<G>(), kMsmSumParts) of
+// T = G::kTree threads.
+template <class G>
+__global__ void __launch_bounds__(G::kTree) k_msm_part_chunks(const typename G::Pt* U,
+                                                               const typename G::Pt* V,
+                                                               typename G::Pt* partial) {
+  using Pt = typename G::Pt;
+  __shared__ Pt sm_pts[G::kTree];
+  constexpr uint32_t chunk = msm_chunk<G>(), chunks = msm_chunks<G>();
   const uint32_t c = blockIdx.x, p = blockIdx.y, tid = threadIdx.x;
   const bool bit_part = p < kMsmPairBits;
-  if (bit_part && c >= kMsmChunks / 2) return;  // whole block exits together
-  g1_xyzz_t acc;
-  {
-    const uint32_t i0 = c * kMsmChunk + 2 * tid;
-    g1_xyzz_t x[2];
+  if (bit_part && c >= chunks / 2) return;  // whole block exits together
+  Pt x[2];
 #pragma unroll
-    for (int k = 0; k < 2; k++) {
-      const uint32_t i = i0 + (uint32_t)k;
-      if (bit_part) {
-        const uint32_t low = i & ((1u << p) - 1u);
-        const uint32_t t = ((i >> p) << (p + 1)) | (1u << p) | low;
-        x[k] = U[t];
-      } else {
-        x[k] = V[i];
-      }
+  for (int k = 0; k < 2; k++) {
+    const uint32_t i = c * chunk + 2 * tid + (uint32_t)k;
+    if (bit_part) {
+      const uint32_t t = ((i >> p) << (p + 1)) | (1u << p) | (i & ((1u << p) - 1u));
+      x[k] = U[t];
+    } else {
+      x[k] = V[i];
     }
-    acc = xyzz_add_nl(x[0], x[1]);
   }
-  sm_pts[tid] = acc;
+  sm_pts[tid] = G::add_nl(x[0], x[1]);
   __syncthreads();
-  for (uint32_t s = 128; s > 0; s >>= 1) {
-    if (tid < s) sm_pts[tid] = xyzz_add_nl(sm_pts[tid], sm_pts[tid + s]);
+  for (uint32_t s = G::kTree / 2; s > 0; s >>= 1) {
+    if (tid < s) sm_pts[tid] = G::add_nl(sm_pts[tid], sm_pts[tid + s]);
     __syncthreads();
   }
-  if (tid == 0) partial[p * kMsmChunks + c] = sm_pts[0];
-}
-
-__device__ __forceinline__ g1_xyzz_t xyzz_shfl_down(const g1_xyzz_t& p, uint32_t d) {
-  g1_xyzz_t o;
-#pragma unroll
-  for (int w = 0; w < 8; w++) {
-    o.x.v[w] = __shfl_down_sync(0xffffffffu, p.x.v[w], d);
-    o.y.v[w] = __shfl_down_sync(0xffffffffu, p.y.v[w], d);
-    o.zz.v[w] = __shfl_down_sync(0xffffffffu, p.zz.v[w], d);
-    o.zzz.v[w] = __shfl_down_sync(0xffffffffu, p.zzz.v[w], d);
-  }
-  return o;
+  if (tid == 0) partial[p * chunks + c] = sm_pts[0];
 }
 
 // Step 8: block p (one warp, a block per part so that each runs on an SM of its own) sums
-// part p's chunks by shuffles and scales the sum: part p < 14 by 2^(p+1), p + 1 doublings.
-// Launch: kMsmSumParts blocks of 32.
-__global__ void __launch_bounds__(32) k_msm_parts(const g1_xyzz_t* partial, g1_xyzz_t* parts) {
+// part p's chunks (lane by lane, then shuffles) and scales the sum: part p < 14 by
+// 2^(p+1), p + 1 doublings. Launch: kMsmSumParts blocks of 32.
+template <class G>
+__global__ void __launch_bounds__(32) k_msm_parts(const typename G::Pt* partial, typename G::Pt* parts) {
+  constexpr uint32_t chunks = msm_chunks<G>();
   const uint32_t lane = threadIdx.x, p = blockIdx.x;
-  const uint32_t n_chunks = p < kMsmPairBits ? kMsmChunks / 2 : kMsmChunks;
-  g1_xyzz_t acc = lane < n_chunks ? partial[p * kMsmChunks + lane] : xyzz_infinity();
+  const uint32_t n_chunks = p < kMsmPairBits ? chunks / 2 : chunks;
+  typename G::Pt acc = G::inf();
+  for (uint32_t c = lane; c < n_chunks; c += 32) acc = G::add_nl(acc, partial[p * chunks + c]);
   for (uint32_t d = 16; d > 0; d >>= 1) {
-    const g1_xyzz_t o = xyzz_shfl_down(acc, d);
-    if (lane < d) acc = xyzz_add_nl(acc, o);
+    const typename G::Pt o = pt_shfl_down(acc, d);
+    if (lane < d) acc = G::add_nl(acc, o);
   }
   if (lane == 0) {
     if (p < kMsmPairBits)
-      for (uint32_t k = 0; k <= p; k++) acc = xyzz_dbl_nl(acc);
+      for (uint32_t k = 0; k <= p; k++) acc = G::dbl_nl(acc);
     parts[p] = acc;
   }
 }
@@ -354,54 +418,58 @@ __global__ void __launch_bounds__(32) k_msm_parts(const g1_xyzz_t* partial, g1_x
 // The sum of the bases whose scalar is 1, beside the bucket path: each thread adds its
 // share (grid-stride, mixed additions of the bases, which are the window-0 table entries),
 // then a tree per block leaves one point per block in partial[blockIdx.x].
-// Launch: any grid of 256 threads.
-__global__ void __launch_bounds__(256) k_msm_ones(const fr_t* scalars, uint32_t n,
-                                                  const g1_aff_t* table, g1_xyzz_t* partial) {
-  __shared__ g1_xyzz_t sm[256];
+// Launch: any grid of G::kTree threads.
+template <class G>
+__global__ void __launch_bounds__(G::kTree) k_msm_ones(const fr_t* scalars, uint32_t n,
+                                                       const typename G::Aff* table,
+                                                       typename G::Pt* partial) {
+  __shared__ typename G::Pt sm[G::kTree];
   const uint32_t stride = gridDim.x * blockDim.x, tid = threadIdx.x;
-  g1_xyzz_t acc = xyzz_infinity();
+  typename G::Pt acc = G::inf();
   for (uint32_t i = blockIdx.x * blockDim.x + tid; i < n; i += stride) {
     const fr_t x = fr_load(scalars + i);
     if (!msm_is_one(x.v)) continue;
-    const g1_aff_t p = table[(size_t)i * kMsmWindows];
-    if (!aff_is_inf(p)) acc = xyzz_madd(acc, p);
+    const typename G::Aff p = table[(size_t)i * kMsmWindows];
+    if (!G::aff_inf(p)) acc = G::madd(acc, p);
   }
   sm[tid] = acc;
   __syncthreads();
-  for (uint32_t d = 128; d > 0; d >>= 1) {
-    if (tid < d) sm[tid] = xyzz_add_nl(sm[tid], sm[tid + d]);
+  for (uint32_t d = G::kTree / 2; d > 0; d >>= 1) {
+    if (tid < d) sm[tid] = G::add_nl(sm[tid], sm[tid + d]);
     __syncthreads();
   }
   if (tid == 0) partial[blockIdx.x] = sm[0];
 }
 
 // The block sums of k_msm_ones (count of them) into one point, parts[kMsmSumParts].
-// Launch: one block of 256.
-__global__ void __launch_bounds__(256) k_msm_ones_sum(const g1_xyzz_t* partial, uint32_t count,
-                                                      g1_xyzz_t* parts) {
-  __shared__ g1_xyzz_t sm[256];
+// Launch: one block of G::kTree.
+template <class G>
+__global__ void __launch_bounds__(G::kTree) k_msm_ones_sum(const typename G::Pt* partial,
+                                                           uint32_t count, typename G::Pt* parts) {
+  __shared__ typename G::Pt sm[G::kTree];
   const uint32_t tid = threadIdx.x;
-  g1_xyzz_t acc = xyzz_infinity();
-  for (uint32_t i = tid; i < count; i += blockDim.x) acc = xyzz_add_nl(acc, partial[i]);
+  typename G::Pt acc = G::inf();
+  for (uint32_t i = tid; i < count; i += blockDim.x) acc = G::add_nl(acc, partial[i]);
   sm[tid] = acc;
   __syncthreads();
-  for (uint32_t d = 128; d > 0; d >>= 1) {
-    if (tid < d) sm[tid] = xyzz_add_nl(sm[tid], sm[tid + d]);
+  for (uint32_t d = G::kTree / 2; d > 0; d >>= 1) {
+    if (tid < d) sm[tid] = G::add_nl(sm[tid], sm[tid + d]);
     __syncthreads();
   }
   if (tid == 0) parts[kMsmSumParts] = sm[0];
 }
 
 // Step 9: Q = the sum of the 15 parts and the ones' sum (shuffles), written in Jacobian
-// coordinates, canonical Montgomery, infinity as (0, 0, 0). Launch: one block of 32.
-__global__ void __launch_bounds__(32) k_msm_final(const g1_xyzz_t* parts, fq_t* out) {
+// coordinates (X, Y, Z), canonical Montgomery, infinity as (0, 0, 0). Launch: one warp.
+template <class G>
+__global__ void __launch_bounds__(32) k_msm_final(const typename G::Pt* parts, typename G::F* out) {
   const uint32_t lane = threadIdx.x;
-  g1_xyzz_t acc = lane <= kMsmSumParts ? parts[lane] : xyzz_infinity();
+  typename G::Pt acc = lane <= kMsmSumParts ? parts[lane] : G::inf();
   for (uint32_t d = 8; d > 0; d >>= 1) {
-    const g1_xyzz_t o = xyzz_shfl_down(acc, d);
-    if (lane < d) acc = xyzz_add_nl(acc, o);
+    const typename G::Pt o = pt_shfl_down(acc, d);
+    if (lane < d) acc = G::add_nl(acc, o);
   }
-  if (lane == 0) xyzz_to_jacobian_t<FqTail>(acc, out[0], out[1], out[2]);
+  if (lane == 0) G::jacobian(acc, out);
 }
 
 }  // namespace g3h

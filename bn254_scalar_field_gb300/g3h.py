@@ -39,7 +39,8 @@ CUDA_STREAM_LEGACY = 0x1
 ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather", "g3h_ntt",
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
                 "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
-                "g3h_compute_h_batch", "g3h_mont_to_std", "g3h_msm_prepare", "g3h_msm")
+                "g3h_compute_h_batch", "g3h_mont_to_std", "g3h_msm_prepare", "g3h_msm",
+                "g3h_msm_g2_prepare", "g3h_msm_g2")
 
 
 class G3HError(RuntimeError):
@@ -81,6 +82,8 @@ def lib():
         L.g3h_mont_to_std.argtypes = [P, P, P, S, U]
         L.g3h_msm_prepare.argtypes = [P, P, U, U]
         L.g3h_msm.argtypes = [P, P, U, P, U]
+        L.g3h_msm_g2_prepare.argtypes = [P, P, U, U]
+        L.g3h_msm_g2.argtypes = [P, P, U, P, U]
         L.g3h_sync.argtypes = [P]
         L.g3h_destroy.argtypes = [P]
         L.g3h_destroy.restype = None
@@ -257,6 +260,25 @@ def g3h_msm(ctx, scalars, result, flags=0):
     _check(lib().g3h_msm(ctx, bufs[0][0], _elems(scalars), bufs[1][0], f), "g3h_msm")
 
 
+def g3h_msm_g2_prepare(ctx, bases, flags=0):
+    """Loads the G2 bases (n, 32) limbs: affine x, y over F_q2, Montgomery over F_q."""
+    if _words(bases) % 32:
+        raise ValueError("bases must hold 32 limbs per point")
+    bufs = [_ptr(bases, None)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_msm_g2_prepare(ctx, bufs[0][0], _words(bases) // 32, f),
+           "g3h_msm_g2_prepare")
+
+
+def g3h_msm_g2(ctx, scalars, result, flags=0):
+    """result (48 limbs: Jacobian X, Y, Z over F_q2) = sum scalars[i] * base[i]."""
+    if _words(result) != 48:
+        raise ValueError("result must hold 48 limbs")
+    bufs = [_ptr(v, None) for v in (scalars, result)]
+    f = _flags(bufs, flags)
+    _check(lib().g3h_msm_g2(ctx, bufs[0][0], _elems(scalars), bufs[1][0], f), "g3h_msm_g2")
+
+
 def g3h_sync(ctx):
     _check(lib().g3h_sync(ctx), "g3h_sync")
 
@@ -343,6 +365,12 @@ class Context:
 
     def msm(self, scalars, result, flags=0):
         g3h_msm(self.handle, scalars, result, flags)
+
+    def msm_g2_prepare(self, bases, flags=0):
+        g3h_msm_g2_prepare(self.handle, bases, flags)
+
+    def msm_g2(self, scalars, result, flags=0):
+        g3h_msm_g2(self.handle, scalars, result, flags)
 
     def sync(self):
         g3h_sync(self.handle)

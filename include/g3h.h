@@ -61,7 +61,7 @@ extern "C" {
                                starting at 0, or a column index >= n_wires */
 #define G3H_E_NOMEM (-4)    /* device or pinned host allocation failed */
 #define G3H_E_CUDA (-5)     /* a CUDA runtime call failed (no device, launch error, ...) */
-#define G3H_E_POINT (-6)    /* a G1 base point is not on the curve y^2 = x^3 + 3 */
+#define G3H_E_POINT (-6)    /* a multiexp base point is not on its curve */
 
 /* flags */
 #define G3H_DEVICE_PTRS 0x1u  /* data pointers of this call are device pointers */
@@ -193,6 +193,17 @@ int g3h_msm_prepare(g3h_ctx* ctx, const uint32_t* bases, uint32_t n_bases, uint3
  * G3H_E_NONCANON unless G3H_NOCHECK. count = 0 writes infinity. */
 int g3h_msm(g3h_ctx* ctx, const uint32_t* scalars, uint32_t count, uint32_t* result,
             uint32_t flags);
+
+/* The same over G2, the twist E': y^2 = x^3 + 3/(9 + u) over F_q2 = F_q[u]/(u^2 + 1)
+ * (EIP-197; MSM_CU stage 7, the witness multiexp of the B query). An F_q2 element is
+ * c0 + c1 u as two F_q elements (16 limbs, c0 first, each Montgomery, canonical); a base is
+ * x then y (32 limbs), (0, 0) the point at infinity; the result is Jacobian (X, Y, Z),
+ * 48 limbs, infinity as zeros. Bases are points of E'(F_q2) (not checked to lie in the
+ * order-r subgroup); each is checked to be canonical and on the twist (G3H_E_POINT).
+ * 2 KiB of prepared data per base. Otherwise as g3h_msm_prepare / g3h_msm. */
+int g3h_msm_g2_prepare(g3h_ctx* ctx, const uint32_t* bases, uint32_t n_bases, uint32_t flags);
+int g3h_msm_g2(g3h_ctx* ctx, const uint32_t* scalars, uint32_t count, uint32_t* result,
+               uint32_t flags);
 
 /* Steps 2-5 like g3h_compute_h_abc, for callers that cannot allocate device memory: a
  * framework whose caching allocator must own every device byte, code running while its

@@ -22,7 +22,7 @@ def L():
 def _declared():
     text = open(os.path.join(ROOT, "include", "g3h.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(g3h_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(g3h_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_entry_points():

@@ -224,3 +224,90 @@ def test_msm_input_checks():
         assert e.value.code == g3h.G3H_E_NONCANON
         ctx.msm(s, res)  # the context is still usable
         assert np.array_equal(_affine(res), oracle.g1_msm(pts, s))
+
+
+# ---------------------------------------------------------------------------- G2 ----
+
+def _affine2(jac):
+    return oracle.g2_jacobian_to_affine(np.asarray(jac, np.uint32).reshape(48))
+
+
+def _oracle_msm2(points, scalars, workers=None):
+    n = points.shape[0]
+    workers = workers or max(1, min(32, os.cpu_count() or 1))
+    if n < 1024 or workers == 1:
+        return oracle.g2_msm(points, scalars)
+    oracle.g2_on_curve(points[:1])
+    bounds = np.linspace(0, n, workers + 1).astype(int)
+    with ThreadPoolExecutor(workers) as ex:
+        parts = list(ex.map(lambda k: oracle.g2_msm(points[bounds[k]:bounds[k + 1]],
+                                                    scalars[bounds[k]:bounds[k + 1]]),
+                            range(workers)))
+    acc = parts[0].reshape(1, 32)
+    for p in parts[1:]:
+        acc = oracle.g2_add(acc, p.reshape(1, 32))
+    return acc.reshape(32)
+
+
+def _run2(points, scalars, device=False):
+    with g3h.Context(0) as ctx:
+        if device:
+            ctx.msm_g2_prepare(_dev(points))
+            res = _dev(np.zeros(48, np.uint32))
+            ctx.msm_g2(_dev(scalars), res)
+            ctx.sync()
+            return _affine2(res.cpu().numpy().view(np.uint32))
+        ctx.msm_g2_prepare(points)
+        res = np.zeros(48, np.uint32)
+        ctx.msm_g2(np.ascontiguousarray(scalars), res)
+        return _affine2(res)
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 300])
+def test_msm_g2_ragged_sizes(n):
+    """The multiexp over the twist (MSM_CU stage 7), host buffers."""
+    from bn254_scalar_field_gb300 import synth_g2
+
+    pts = synth_g2.points(n, seed=1000 + n)
+    s = synth_g1.scalars(n, seed=1100 + n)
+    if n == 300:
+        s[:4] = F.ints_to_array([0, 1, R - 1, (1 << 15) + 1])
+    assert np.array_equal(_run2(pts, s), oracle.g2_msm(pts, s))
+
+
+def test_msm_g2_witness_and_full_size():
+    """A witness as scalars (mostly 0 and 1) on 4096 twist points, device buffers, and
+    uniform scalars on 2^16 points."""
+    from bn254_scalar_field_gb300 import synth_g2
+
+    _, _, w = synth.problem(12)
+    pts = synth_g2.points(w.shape[0], seed=1200)
+    ws = oracle.from_mont(w)
+    assert np.array_equal(_run2(pts, ws, device=True), _oracle_msm2(pts, ws))
+    n = 1 << 16
+    pts = synth_g2.points(n, seed=synth_g2.default_seed(16))
+    s = synth_g1.scalars(n, seed=synth_g2.default_seed(16) + 1)
+    assert np.array_equal(_run2(pts, s, device=True), _oracle_msm2(pts, s))
+
+
+def test_msm_g2_cancellation_and_checks():
+    from bn254_scalar_field_gb300 import synth_g2
+    from oracle import g2_int as G2
+
+    base = synth_g2.points(6, seed=1300)  # base[1] = -base[0]
+    pts = np.concatenate([np.repeat(base[:1], 20, axis=0), base[:2], np.zeros((2, 32), np.uint32)])
+    s = synth_g1.scalars(pts.shape[0], seed=1301)
+    s[:20] = s[0]
+    s[20:22] = s[5]
+    assert np.array_equal(_run2(pts, s), oracle.g2_msm(pts, s))
+    with g3h.Context(0) as ctx:
+        bad = base.copy()
+        bad[2, 16] ^= 1
+        with pytest.raises(g3h.G3HError) as e:
+            ctx.msm_g2_prepare(bad)
+        assert e.value.code == g3h.G3H_E_POINT
+        bad = base.copy()
+        bad[3, 8:16] = F.int_to_limbs(G2.Q_MOD)
+        with pytest.raises(g3h.G3HError) as e:
+            ctx.msm_g2_prepare(bad)
+        assert e.value.code == g3h.G3H_E_NONCANON
