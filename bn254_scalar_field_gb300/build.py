@@ -35,6 +35,20 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
+def h_path_digest():
+    """SHA-256 (first 16 hex digits) of the device code of the H path's kernels (field
+    arithmetic, NTT slices, gather and join): recorded next to their profiler counters, so
+    that figures taken on other kernels are not reused, while changes elsewhere (host code,
+    the multiexp) keep them valid."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("fr.cuh", "ntt.cuh", "kernels.cuh"):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def is_fresh():
     if not os.path.exists(LIB_PATH):
         return False
