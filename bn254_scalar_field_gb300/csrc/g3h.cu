@@ -1,15 +1,21 @@
 // The C ABI of include/g3h.h: context, resident tables, launch plans.
 //
 // Work per H computation on a domain of 2^k >= 2^6 points (two slice levels, k = lo + hi;
-// three levels for k > 22; a slice is at most 2^11 elements):
-//   k_ntt_dif  (3 vectors)   inverse passes on the top bits, strided slices; for
-//                            compute_h the gather forms a, b, c in its load
-//                            (compute_h_abc loads them)
-//   k_ntt_mid  (3 vectors)   inverse passes on the low bits, shift g^brev(p)/n, forward
+// three levels for k > 22; a slice is at most 2^11 elements), per vector a, b, c:
+//   k_gather_rows  (a, b)    the CSR rows of A and of B against the witness
+//   k_ntt_dif                inverse passes on the top bits, strided slices; for c the
+//                            load forms c = a * b (compute_h_abc loads a, b, c)
+//   k_ntt_mid                inverse passes on the low bits, shift g^brev(p)/n, forward
 //                            passes on the low bits, contiguous slices
-//   k_ntt_dit  (join)        forward passes on the top bits for a, b, then c with
-//                            h = a*b - c written in both encodings at c's store
-// All launches go to the context's stream in order; nothing synchronises between them.
+//   k_ntt_dit                forward passes on the top bits
+//   k_join                   h = a*b - c in both encodings
+// The three vectors' kernels run on three streams (fork/join events), the whole sequence
+// captured once into a CUDA graph per set of pointers and replayed; G3H_SERIALIZE runs the
+// three vectors as one launch per phase on one stream, G3H_FUSED_JOIN writes h from the last
+// forward kernel instead of k_join. Slice kernels come in two builds (ntt.cuh, SliceCfg):
+// radix-4 pass pairs for 2^9 and 2^10 slices, radix-2 passes otherwise.
+//
+// The multiexps over G1 and G2 (msm.cuh) keep their prepared bases in the context.
 #include <cuda_runtime.h>
 
 #include <algorithm>
