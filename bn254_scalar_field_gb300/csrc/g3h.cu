@@ -137,7 +137,7 @@ struct MsmState {
   uint32_t slots = 0;                // resident threads of the accumulation kernel
   void* table = nullptr;             // 16 affine points per base: 2^(16 w) P_i
   uint32_t* entries = nullptr;       // 16 per base
-  uint32_t* counts = nullptr;        // per bucket
+  uint32_t* counts = nullptr;        // per bucket | long-run list (count, indices)
   uint32_t* offsets = nullptr;       // per bucket + 1
   uint32_t* cursor = nullptr;        // per bucket
   void* buckets = nullptr;           // per bucket
@@ -1030,7 +1030,8 @@ int msm_launches(g3h_ctx* c, MsmState& m, const fr_t* s, uint32_t count, typenam
   constexpr uint32_t T = G::kTree;
   constexpr uint32_t chunks = msm_chunks<G>();
   cudaStream_t st = c->stream;
-  if (cudaMemsetAsync(m.counts, 0, kMsmBuckets * sizeof(uint32_t), st) != cudaSuccess)
+  // the counters and the long-run list's count start at zero
+  if (cudaMemsetAsync(m.counts, 0, (kMsmBuckets + 1) * sizeof(uint32_t), st) != cudaSuccess)
     return G3H_E_CUDA;
   const unsigned grid = (unsigned)std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
   const Aff* table = (const Aff*)m.table;
@@ -1080,9 +1081,17 @@ int msm_launches(g3h_ctx* c, MsmState& m, const fr_t* s, uint32_t count, typenam
       k_msm_accumulate<G><<<blocks_for(n_slices, T), T, 0, st>>>(
           m.entries, m.offsets, table, buckets, head, tail, n_slices);
     });
+  // the list of buckets with long runs (count first) lives after the scan's counters
+  uint32_t* long_list = m.counts + kMsmBuckets;
   if (rc == G3H_OK)
     rc = run(c, "msm_merge", [&] {
-      k_msm_merge<G><<<kMsmBuckets / 128, 128, 0, st>>>(m.offsets, buckets, head, tail, n_slices);
+      k_msm_merge<G><<<kMsmBuckets / 128, 128, 0, st>>>(m.offsets, buckets, head, tail, n_slices,
+                                                         long_list);
+    });
+  if (rc == G3H_OK)
+    rc = run(c, "msm_merge_long", [&] {
+      k_msm_merge_long<G><<<(unsigned)c->sm_count, T, 0, st>>>(m.offsets, buckets, head, tail,
+                                                               n_slices, long_list);
     });
   Pt* U = (Pt*)m.groups;
   Pt* V = U + kMsmPairs;
@@ -1121,7 +1130,8 @@ int msm_prepare(g3h_ctx* c, MsmState& m, const uint32_t* bases, uint32_t n_bases
   };
   int rc = alloc(&m.table, n * kMsmWindows * sizeof(Aff));
   if (rc == G3H_OK) rc = dalloc(&m.entries, n * kMsmWindows);
-  if (rc == G3H_OK) rc = dalloc(&m.counts, kMsmBuckets);
+  // per-bucket counters, then the long-run list: its count and up to kMsmBuckets indices
+  if (rc == G3H_OK) rc = dalloc(&m.counts, 2 * kMsmBuckets + 1);
   if (rc == G3H_OK) rc = dalloc(&m.offsets, kMsmBuckets + 1);
   if (rc == G3H_OK) rc = dalloc(&m.cursor, kMsmBuckets);
   if (rc == G3H_OK) rc = alloc(&m.buckets, kMsmBuckets * sizeof(Pt));

@@ -21,7 +21,8 @@
 //      that lies inside one slice is written to its bucket, a run cut by a slice boundary
 //      leaves its part in that slice's head or tail slot (MSM_CU, "the load-balanced
 //      form": segmented accumulation with boundary spills);
-//   5. merge: a cut bucket sums its parts from the slices its run covers;
+//   5. merge: a cut bucket sums its parts from the slices its run covers (one thread per
+//      bucket; a block per bucket for runs over many slices);
 //   6-8. the weighted sum sum_j j B_j: per pair of buckets (t = 0 .. 16383) U_t and V_t;
 //      then Q = sum_t V_t + sum_b 2^(b+1) sum_{t : bit b of t} U_t, fourteen bit-sums and
 //      one sum of V reduced by trees over all SMs, scaled by doublings (one SM per part)
@@ -311,11 +312,16 @@ __global__ void __launch_bounds__(G::kTree) k_msm_accumulate(
 
 // Step 5: one thread per bucket. A bucket with no entries is set to infinity; a run cut by
 // slice boundaries is the tail part of its first slice plus the head parts of the rest.
-// Launch: kMsmBuckets / 128 blocks of 128.
+// A run over more than kMsmMergeSerial slices (a value repeated in many scalars puts all
+// its digits in one bucket) is left to k_msm_merge_long: its index goes to long_list.
+// Launch: kMsmBuckets / 128 blocks of 128; long_list[0] (the count) zero beforehand.
+constexpr uint32_t kMsmMergeSerial = 16;
+
 template <class G>
 __global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, typename G::Pt* buckets,
                                                    const typename G::Pt* head,
-                                                   const typename G::Pt* tail, uint32_t n_slices) {
+                                                   const typename G::Pt* tail, uint32_t n_slices,
+                                                   uint32_t* long_list) {
   const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= kMsmBuckets) return;
   const uint32_t slice = msm_slice_len(offsets[kMsmBuckets], n_slices);
@@ -326,9 +332,42 @@ __global__ void __launch_bounds__(128) k_msm_merge(const uint32_t* offsets, type
   }
   const uint32_t k_lo = s / slice, k_hi = (e - 1u) / slice;
   if (k_lo == k_hi) return;
+  if (k_hi - k_lo > kMsmMergeSerial) {
+    long_list[1 + atomicAdd(long_list, 1u)] = j;
+    return;
+  }
   typename G::Pt acc = tail[k_lo];
   for (uint32_t k = k_lo + 1; k <= k_hi; k++) acc = G::add(acc, head[k]);
   buckets[j] = acc;
+}
+
+// Step 5 for the long runs: one block per listed bucket (grid-stride over the list), its
+// threads sum the head parts by strides, a tree in shared memory adds them and the first
+// slice's tail part. Launch: any grid of G::kTree threads.
+template <class G>
+__global__ void __launch_bounds__(G::kTree) k_msm_merge_long(const uint32_t* offsets,
+                                                             typename G::Pt* buckets,
+                                                             const typename G::Pt* head,
+                                                             const typename G::Pt* tail,
+                                                             uint32_t n_slices,
+                                                             const uint32_t* long_list) {
+  __shared__ typename G::Pt sm[G::kTree];
+  const uint32_t tid = threadIdx.x, count = long_list[0];
+  const uint32_t slice = msm_slice_len(offsets[kMsmBuckets], n_slices);
+  for (uint32_t d = blockIdx.x; d < count; d += gridDim.x) {
+    const uint32_t j = long_list[1 + d];
+    const uint32_t k_lo = offsets[j] / slice, k_hi = (offsets[j + 1] - 1u) / slice;
+    typename G::Pt acc = tid == 0 ? tail[k_lo] : G::inf();
+    for (uint32_t k = k_lo + 1 + tid; k <= k_hi; k += blockDim.x) acc = G::add_nl(acc, head[k]);
+    sm[tid] = acc;
+    __syncthreads();
+    for (uint32_t w = G::kTree / 2; w > 0; w >>= 1) {
+      if (tid < w) sm[tid] = G::add_nl(sm[tid], sm[tid + w]);
+      __syncthreads();
+    }
+    if (tid == 0) buckets[j] = sm[0];
+    __syncthreads();  // sm is reused by the next listed bucket
+  }
 }
 
 // The weighted sum Q = sum_j (j + 1) B_j. With pairs t = (B_2t, B_2t+1), digits 2t + 1 and

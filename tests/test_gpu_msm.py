@@ -128,6 +128,17 @@ def test_msm_one_scalar_for_all_bases():
     assert np.array_equal(_run(pts, s), _oracle_msm(pts, s))
 
 
+def test_msm_repeated_scalar_long_runs():
+    """Most scalars equal to 2 (not 1): all their digits land in one bucket whose run covers
+    hundreds of slices, which the merge hands to a block per bucket."""
+    n = 1 << 15
+    pts = synth_g1.points(n, seed=31)
+    s = synth_g1.scalars(n, seed=32)
+    two = F.ints_to_array([2])[0]
+    s[np.arange(n) % 5 != 0] = two
+    assert np.array_equal(_run(pts, s, device=True), _oracle_msm(pts, s))
+
+
 def test_msm_exceptional_additions():
     """Equal bases with equal scalars meet in one bucket (the mixed addition's doubling
     case); P and -P with equal scalars cancel; bases at infinity add nothing."""
