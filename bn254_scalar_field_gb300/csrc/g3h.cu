@@ -271,6 +271,15 @@ enum class Slice { dif, mid, dit, brev };
 // per butterfly of a radix-2 pass, one per group of four of a radix-4 pass pair, up to
 // the build's block size.
 void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
+  if (kk >= kCfg2MinSliceBits) {
+    *threads = std::min(1u << (kk - 2u), SliceCfg<2>::threads);
+    switch (which) {
+      case Slice::dif: return k_ntt_dif<2>;
+      case Slice::mid: return k_ntt_mid<2>;
+      case Slice::dit: return k_ntt_dit<2>;
+      default: break;
+    }
+  }
   const bool r4 = kk >= kRadix4MinSliceBits && kk <= kRadix4MaxSliceBits && kk >= 2;
   *threads = r4 ? std::min(1u << (kk - 2u), SliceCfg<1>::threads)
                 : std::min(1u << (kk - 1u), SliceCfg<0>::threads);
@@ -298,7 +307,8 @@ int launch_slice(g3h_ctx* c, const char* name, Slice which, const SliceArgs& a, 
 int set_smem_limits() {
   const int bytes = 32 << 11;  // the largest slice, 2^11 elements
   void (*kerns[])(SliceArgs) = {k_ntt_dif<0>, k_ntt_mid<0>, k_ntt_dit<0>, k_ntt_dif<1>,
-                                k_ntt_mid<1>, k_ntt_dit<1>, k_ntt_brev};
+                                k_ntt_mid<1>, k_ntt_dit<1>, k_ntt_dif<2>, k_ntt_mid<2>,
+                                k_ntt_dit<2>, k_ntt_brev};
   for (auto k : kerns)
     if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)

@@ -129,19 +129,9 @@ __device__ __forceinline__ fr_t gather_c(const fr_t& a, const fr_t& b) {
   return (fr_is_zero(a) || fr_is_zero(b)) ? fr_zero() : fr_canon(fr_mul(a, b));
 }
 
-// Threads of a slice kernel: one per butterfly up to kSliceThreads.
-#ifndef G3H_SLICE_THREADS
-#define G3H_SLICE_THREADS 256
-#endif
-constexpr uint32_t kSliceThreads = G3H_SLICE_THREADS;
-#ifndef G3H_PASS_UNROLL
-#define G3H_PASS_UNROLL 1
-#endif
-constexpr int kPassUnroll = G3H_PASS_UNROLL;
-// Four resident blocks of 256 threads per SM (up to 64 registers each) measured best.
-#ifndef G3H_SLICE_MIN_BLOCKS
-#define G3H_SLICE_MIN_BLOCKS 4
-#endif
+// Threads of the radix-2 k_ntt_brev kernel: one per butterfly up to kSliceThreads, four
+// resident blocks per SM. The other slice kernels' builds: SliceCfg below.
+constexpr uint32_t kSliceThreads = 256;
 
 // Butterfly of the pass on slice bit lb: index bf in [0, 2^(kk-1)) -> lower element lo,
 // upper element lo + 2^lb, and the twiddle table index of the element bit c0 + lb:
@@ -179,7 +169,7 @@ __device__ __forceinline__ Bfly bfly_at(uint32_t bf, uint32_t lb, uint32_t kk, u
 __device__ __forceinline__ void dif_pass(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
                                          uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
   const uint32_t size = 1u << kk;
-#pragma unroll kPassUnroll
+#pragma unroll 1
   for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
     const Bfly b = bfly_at(bf, lb, kk, low, c0, k);
     const fr_t u = sm_get(sm, size, b.lo), v = sm_get(sm, size, b.hi);
@@ -195,7 +185,7 @@ __device__ __forceinline__ void dif_pass(uint4* sm, uint32_t kk, const fr_const_
 __device__ __forceinline__ void dit_pass(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
                                          uint32_t lb, uint32_t low, uint32_t c0, uint32_t k) {
   const uint32_t size = 1u << kk;
-#pragma unroll kPassUnroll
+#pragma unroll 1
   for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
     const Bfly b = bfly_at(bf, lb, kk, low, c0, k);
     fr_t v = sm_get(sm, size, b.hi);
@@ -320,12 +310,13 @@ __device__ __forceinline__ void dit_passes(uint4* sm, uint32_t kk, const fr_cons
   for (; lb < kk; lb++) dit_pass(sm, kk, tw, lb, low, c0, k);
 }
 
-// Two builds of each slice kernel. Configuration 1: radix-4 pass pairs, 128 threads,
-// five resident blocks per SM (up to 102 registers); configuration 0: radix-2 passes,
-// 256 threads, four blocks (64 registers). Measured on GB300: 1 is faster on slices of
-// 2^9 and 2^10 elements (2^18 H: 0.310 -> 0.295 ms; 2^20: 1.146 -> 1.071 ms), 0 on
-// smaller slices (2^12, 2^14: latency-bound, 0.069 vs 0.081 ms) and on the 2^11 slices of
-// 2^22 (4.97 vs 5.18 ms).
+// Three builds of each slice kernel, chosen by slice size (measured on GB300):
+//   0: radix-2 passes, 256 threads, four resident blocks per SM (64 registers): slices up
+//      to 2^8 (2^12, 2^14: latency-bound, the pass pairs measured 0.069 -> 0.081 ms);
+//   1: radix-4 pass pairs, 128 threads, five blocks (up to 102 registers): 2^9 and 2^10
+//      slices (2^18 H: 0.310 -> 0.295 ms; 2^20: 1.146 -> 1.071 ms);
+//   2: radix-4 pass pairs, 256 threads, three blocks (85 registers; three 64 KiB slices
+//      fill the shared memory): 2^11 slices (2^22 H: 4.97 -> 4.81 ms; build 1 there: 5.18).
 template <int C>
 struct SliceCfg;
 template <>
@@ -338,13 +329,12 @@ struct SliceCfg<1> {
   static constexpr bool r4 = true;
   static constexpr uint32_t threads = 128, min_blocks = 5;
 };
-#ifndef G3H_R4_MIN_BITS
-#define G3H_R4_MIN_BITS 9
-#endif
-#ifndef G3H_R4_MAX_BITS
-#define G3H_R4_MAX_BITS 10
-#endif
-constexpr uint32_t kRadix4MinSliceBits = G3H_R4_MIN_BITS, kRadix4MaxSliceBits = G3H_R4_MAX_BITS;
+template <>
+struct SliceCfg<2> {
+  static constexpr bool r4 = true;
+  static constexpr uint32_t threads = 256, min_blocks = 3;
+};
+constexpr uint32_t kRadix4MinSliceBits = 9, kRadix4MaxSliceBits = 10, kCfg2MinSliceBits = 11;
 
 // Block s of a strided slice kernel owns low = s mod 2^c0, high = s >> c0 and the
 // elements low + (m << c0) + (high << (c0 + kk)), m < 2^kk.
@@ -491,7 +481,7 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 // page), scaled by scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and
 // the result goes to dst (out of place: a block reads other blocks' elements).
 // Launch: grid (n >> kk), block min(2^(kk-1), 256), shared 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads, G3H_SLICE_MIN_BLOCKS) k_ntt_brev(const __grid_constant__ SliceArgs p) {
+__global__ void __launch_bounds__(kSliceThreads, 4) k_ntt_brev(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
