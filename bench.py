@@ -358,10 +358,10 @@ def main():
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             rec = json.load(f)
-        from bn254_scalar_field_gb300.build import h_path_digest
+        from bn254_scalar_field_gb300.build import kernel_digest
 
         ent = rec.get(top)
-        if ent and ent.get("kernel_digest") == h_path_digest() and ent.get("log_n") == LOG_N:
+        if ent and ent.get("kernel_digest") == kernel_digest(top) and ent.get("log_n") == LOG_N:
             traffic = ent["bytes_per_launch"]
     except (OSError, ValueError, ImportError):
         pass

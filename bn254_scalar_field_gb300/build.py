@@ -35,15 +35,18 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def h_path_digest():
-    """SHA-256 (first 16 hex digits) of the device code of the H path's kernels (field
-    arithmetic, NTT slices, gather and join): recorded next to their profiler counters, so
-    that figures taken on other kernels are not reused, while changes elsewhere (host code,
-    the multiexp) keep them valid."""
+def kernel_digest(kernel):
+    """SHA-256 (first 16 hex digits) of the device code a profiled H-path kernel is built
+    from (the NTT slice kernels: field arithmetic and ntt.cuh; the gather and join also
+    kernels.cuh): recorded next to its profiler counters, so that figures taken on other
+    code are not reused, while changes elsewhere keep them valid."""
     import hashlib
 
+    files = ["fr.cuh", "ntt.cuh"]
+    if not kernel.startswith("ntt_"):
+        files.append("kernels.cuh")
     h = hashlib.sha256()
-    for f in ("fr.cuh", "ntt.cuh", "kernels.cuh"):
+    for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
