@@ -206,6 +206,20 @@ def cpu_baseline(A, B, w, budget_s=12.0, max_runs=20):
     out = {"value": runs / total, "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": "%d whole 2^18 H computations (%.1f s), C oracle, one thread" % (
                runs, total)}
+    # the same oracle on every host core: independent H computations on host threads (the
+    # C calls release the interpreter lock), the aggregate rate
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = max(1, os.cpu_count() or 1)
+    per = max(1, int(round(budget_s / 2 / max(total / runs, 1e-3))))
+    t = time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        list(ex.map(lambda _: oracle.compute_h(LOG_N, A, B, w), range(cores * per)))
+    dt = time.perf_counter() - t
+    out["all_cores_value"] = cores * per / dt
+    out["all_cores"] = cores
+    out["all_cores_sample"] = "%d whole 2^18 H computations on %d threads (%.1f s)" % (
+        cores * per, cores, dt)
     # the H multiexp's oracle (double-and-add per point) on a sample of the 2^18 bases,
     # as points per second, beside the GPU's msm_2^18_per_s * 2^18
     from bn254_scalar_field_gb300 import synth_g1
