@@ -49,6 +49,20 @@ __device__ __forceinline__ fq2_t fq2_sqr_t(const fq2_t& a) {
   return {M::mul(fq_add(a.c0, a.c1), fq_sub(a.c0, a.c1)), fq_dbl(t)};
 }
 
+// F_q2 products as out-of-line calls with their F_q multiplies inlined: one call per F_q2
+// product, whose three (two for a square) independent F_q products interleave.
+__device__ __noinline__ fq2_t fq2_mul_call(fq2_t a, fq2_t b) { return fq2_mul_t<FqInline>(a, b); }
+__device__ __noinline__ fq2_t fq2_sqr_call(fq2_t a) { return fq2_sqr_t<FqInline>(a); }
+struct Fq2Call {};
+template <>
+__device__ __forceinline__ fq2_t fq2_mul_t<Fq2Call>(const fq2_t& a, const fq2_t& b) {
+  return fq2_mul_call(a, b);
+}
+template <>
+__device__ __forceinline__ fq2_t fq2_sqr_t<Fq2Call>(const fq2_t& a) {
+  return fq2_sqr_call(a);
+}
+
 // 1 / (a0 + a1 u) = (a0 - a1 u) / (a0^2 + a1^2); 0 maps to 0.
 __device__ __forceinline__ fq2_t fq2_inv(const fq2_t& a) {
   const fq_t ni = fq_inv(fq_add(fq_mul(a.c0, a.c0), fq_mul(a.c1, a.c1)));

@@ -139,7 +139,8 @@ struct MsmState {
   uint32_t* entries = nullptr;       // 16 per base
   uint32_t* counts = nullptr;        // per bucket | long-run list (count, indices)
   uint32_t* offsets = nullptr;       // per bucket + 1
-  uint32_t* cursor = nullptr;        // per bucket
+  uint32_t sort_blocks = 0;          // blocks of the counting sort (one per SM)
+  uint32_t* block_counts = nullptr;  // per sort block and bucket
   void* buckets = nullptr;           // per bucket
   void* spill = nullptr;             // head | tail parts, (n + 1) each
   void* groups = nullptr;            // U | V, kMsmPairs each
@@ -200,7 +201,7 @@ int dalloc(T** p, size_t count) {
 }
 
 void msm_free(MsmState& m) {
-  void* bufs[] = {m.table, m.entries, m.counts, m.offsets, m.cursor,
+  void* bufs[] = {m.table, m.entries, m.counts, m.offsets, m.block_counts,
                   m.buckets, m.spill, m.groups, m.parts, m.result};
   for (void* b : bufs)
     if (b) cudaFree(b);
@@ -311,6 +312,12 @@ int set_smem_limits() {
                                 k_ntt_dit<2>, k_ntt_brev};
   for (auto k : kerns)
     if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return G3H_E_CUDA;
+  // the multiexp's counting sort: a counter per bucket in each block
+  const void* sort_kerns[] = {(const void*)k_msm_count, (const void*)k_msm_scatter};
+  for (auto k : sort_kerns)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMsmSortSmem) !=
         cudaSuccess)
       return G3H_E_CUDA;
   return G3H_OK;
@@ -1040,10 +1047,13 @@ int msm_launches(g3h_ctx* c, MsmState& m, const fr_t* s, uint32_t count, typenam
   constexpr uint32_t T = G::kTree;
   constexpr uint32_t chunks = msm_chunks<G>();
   cudaStream_t st = c->stream;
-  // the counters and the long-run list's count start at zero
-  if (cudaMemsetAsync(m.counts, 0, (kMsmBuckets + 1) * sizeof(uint32_t), st) != cudaSuccess)
+  // the long-run list's count starts at zero
+  if (cudaMemsetAsync(m.counts + kMsmBuckets, 0, sizeof(uint32_t), st) != cudaSuccess)
     return G3H_E_CUDA;
-  const unsigned grid = (unsigned)std::min<size_t>(blocks_for(count, 256), (size_t)c->sm_count * 8);
+  // sort blocks: one per SM, fewer for few scalars; block b owns scalars [b chunk, ...)
+  const uint32_t sort_blocks = std::max<uint32_t>(
+      1u, std::min<uint32_t>(m.sort_blocks, (count + kMsmSortThreads - 1) / kMsmSortThreads));
+  const uint32_t sort_chunk = (count + sort_blocks - 1) / sort_blocks;
   const Aff* table = (const Aff*)m.table;
   Pt* buckets = (Pt*)m.buckets;
   Pt* chunk_sums = (Pt*)m.parts;
@@ -1067,15 +1077,22 @@ int msm_launches(g3h_ctx* c, MsmState& m, const fr_t* s, uint32_t count, typenam
     });
   if (rc == G3H_OK && cudaEventRecord(ln.ev_end[0], os) != cudaSuccess) rc = G3H_E_CUDA;
   if (rc == G3H_OK) rc = run(c, "msm_count", [&] {
-    k_msm_count<<<grid, 256, 0, st>>>(s, count, m.counts, check, c->d_err);
+    k_msm_count<<<sort_blocks, kMsmSortThreads, kMsmSortSmem, st>>>(s, count, sort_chunk,
+                                                                    m.block_counts, check,
+                                                                    c->d_err);
   });
   if (rc == G3H_OK)
+    rc = run(c, "msm_count_cols", [&] {
+      k_msm_count_cols<<<kMsmBuckets / 32, 256, 0, st>>>(m.block_counts, sort_blocks, m.counts);
+    });
+  if (rc == G3H_OK)
     rc = run(c, "msm_scan", [&] {
-      k_msm_scan<<<1, 1024, 0, st>>>(m.counts, m.offsets, m.cursor);
+      k_msm_scan<<<1, 1024, 0, st>>>(m.counts, m.offsets);
     });
   if (rc == G3H_OK)
     rc = run(c, "msm_scatter", [&] {
-      k_msm_scatter<<<grid, 256, 0, st>>>(s, count, m.cursor, m.entries);
+      k_msm_scatter<<<sort_blocks, kMsmSortThreads, kMsmSortSmem, st>>>(
+          s, count, sort_chunk, m.offsets, m.block_counts, m.entries);
     });
   // threads for slices of equal length, about one per resident thread of the accumulation
   // kernel for the most entries there can be; the kernels size the slices to the entries
@@ -1143,7 +1160,8 @@ int msm_prepare(g3h_ctx* c, MsmState& m, const uint32_t* bases, uint32_t n_bases
   // per-bucket counters, then the long-run list: its count and up to kMsmBuckets indices
   if (rc == G3H_OK) rc = dalloc(&m.counts, 2 * kMsmBuckets + 1);
   if (rc == G3H_OK) rc = dalloc(&m.offsets, kMsmBuckets + 1);
-  if (rc == G3H_OK) rc = dalloc(&m.cursor, kMsmBuckets);
+  m.sort_blocks = (uint32_t)c->sm_count;
+  if (rc == G3H_OK) rc = dalloc(&m.block_counts, (size_t)m.sort_blocks * kMsmBuckets);
   if (rc == G3H_OK) rc = alloc(&m.buckets, kMsmBuckets * sizeof(Pt));
   if (rc == G3H_OK) rc = alloc(&m.spill, 2 * (n + 1) * sizeof(Pt));
   if (rc == G3H_OK) rc = alloc(&m.groups, 2 * kMsmPairs * sizeof(Pt));
