@@ -177,7 +177,9 @@ int g3h_mont_to_std(g3h_ctx* ctx, const uint32_t* in, uint32_t* out, size_t coun
 /* Loads n_bases G1 bases into the context (replacing any loaded before) and prepares them:
  * for each base P the 16 points 2^(16 w) P, w < 16, are computed on the device and kept
  * resident (1 KiB per base; 256 MiB for 2^18 bases), so that every later g3h_msm needs
- * one bucket pass for all its windows. `bases`: 16 * n_bases limbs, host memory, or device
+ * one bucket pass for all its windows. Scratch for the multiexp is allocated here too:
+ * 320 bytes per base (576 for G2) and about 30 MiB independent of n_bases (among it a
+ * 128 KiB bucket-counter array per SM for the sort of the window digits). `bases`: 16 * n_bases limbs, host memory, or device
  * memory with G3H_DEVICE_PTRS (read only during the call). n_bases <= 2^G3H_MSM_MAX_LOG.
  * Synchronous. Returns G3H_E_NONCANON (a coordinate >= q), G3H_E_POINT (a base off the
  * curve), G3H_E_RANGE, G3H_E_NOMEM; on error no bases are loaded. n_bases = 0 unloads. */
