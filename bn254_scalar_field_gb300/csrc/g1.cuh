@@ -26,13 +26,44 @@ struct __align__(16) g1_xyzz_t {
 // out-of-line copy. A point addition inlines 14 multiplies (some 30 KB of code), more than
 // the instruction cache keeps; where few warps run, as in the bucket sum, they stall on
 // instruction fetch, and calling one compact multiply is faster.
+//
+// mul2 takes two independent products (x = a b, y = c d). FqPair computes them in one
+// out-of-line call whose two inlined multiplies interleave, so that a lone warp waits on
+// the latency of about one multiply for both.
 struct FqInline {
   static __device__ __forceinline__ fq_t mul(const fq_t& a, const fq_t& b) { return fq_mul(a, b); }
+  static __device__ __forceinline__ void mul2(const fq_t& a, const fq_t& b, const fq_t& c,
+                                              const fq_t& d, fq_t& x, fq_t& y) {
+    x = fq_mul(a, b);
+    y = fq_mul(c, d);
+  }
 };
 __device__ __noinline__ fq_t fq_mul_call(fq_t a, fq_t b) { return fq_mul(a, b); }
 struct FqCall {
   static __device__ __forceinline__ fq_t mul(const fq_t& a, const fq_t& b) {
     return fq_mul_call(a, b);
+  }
+  static __device__ __forceinline__ void mul2(const fq_t& a, const fq_t& b, const fq_t& c,
+                                              const fq_t& d, fq_t& x, fq_t& y) {
+    x = fq_mul_call(a, b);
+    y = fq_mul_call(c, d);
+  }
+};
+struct fq_pair_t {
+  fq_t x, y;
+};
+__device__ __noinline__ fq_pair_t fq_mul2_call(fq_t a, fq_t b, fq_t c, fq_t d) {
+  return {fq_mul(a, b), fq_mul(c, d)};
+}
+struct FqPair {
+  static __device__ __forceinline__ fq_t mul(const fq_t& a, const fq_t& b) {
+    return fq_mul_call(a, b);
+  }
+  static __device__ __forceinline__ void mul2(const fq_t& a, const fq_t& b, const fq_t& c,
+                                              const fq_t& d, fq_t& x, fq_t& y) {
+    const fq_pair_t r = fq_mul2_call(a, b, c, d);
+    x = r.x;
+    y = r.y;
   }
 };
 
@@ -69,15 +100,15 @@ __device__ __forceinline__ g1_xyzz_t xyzz_from_aff(const g1_aff_t& a) {
 template <class M>
 __device__ __forceinline__ g1_xyzz_t xyzz_dbl_t(const g1_xyzz_t& p) {
   const fq_t u = fq_dbl(p.y);
-  const fq_t v = M::mul(u, u);
-  const fq_t w = M::mul(u, v);
-  const fq_t s = M::mul(p.x, v);
-  const fq_t xx = M::mul(p.x, p.x);
+  fq_t v, xx, w, s, mm, my, wy;
+  M::mul2(u, u, p.x, p.x, v, xx);
+  M::mul2(u, v, p.x, v, w, s);
   const fq_t m = fq_add(fq_dbl(xx), xx);
   g1_xyzz_t r;
-  r.x = fq_sub(M::mul(m, m), fq_dbl(s));
-  r.y = fq_sub(M::mul(m, fq_sub(s, r.x)), M::mul(w, p.y));
-  r.zz = M::mul(v, p.zz);
+  M::mul2(m, m, v, p.zz, mm, r.zz);
+  r.x = fq_sub(mm, fq_dbl(s));
+  M::mul2(m, fq_sub(s, r.x), w, p.y, my, wy);
+  r.y = fq_sub(my, wy);
   r.zzz = M::mul(w, p.zzz);
   return r;
 }
@@ -134,24 +165,24 @@ template <class M>
 __device__ __forceinline__ g1_xyzz_t xyzz_add_t(const g1_xyzz_t& a, const g1_xyzz_t& b) {
   if (xyzz_is_inf(a)) return b;
   if (xyzz_is_inf(b)) return a;
-  const fq_t u1 = M::mul(a.x, b.zz);
-  const fq_t u2 = M::mul(b.x, a.zz);
-  const fq_t s1 = M::mul(a.y, b.zzz);
-  const fq_t s2 = M::mul(b.y, a.zzz);
+  fq_t u1, u2, s1, s2;
+  M::mul2(a.x, b.zz, b.x, a.zz, u1, u2);
+  M::mul2(a.y, b.zzz, b.y, a.zzz, s1, s2);
   const fq_t p = fq_sub(u2, u1);
   const fq_t r = fq_sub(s2, s1);
   if (fq_is_zero(p)) {
     if (fq_is_zero(r)) return xyzz_dbl_t<M>(a);
     return xyzz_infinity();
   }
-  const fq_t pp = M::mul(p, p);
-  const fq_t ppp = M::mul(p, pp);
-  const fq_t q = M::mul(u1, pp);
+  fq_t pp, rr, ppp, q, zz12, zzz12, ry, sp;
+  M::mul2(p, p, r, r, pp, rr);
+  M::mul2(p, pp, u1, pp, ppp, q);
+  M::mul2(a.zz, b.zz, a.zzz, b.zzz, zz12, zzz12);
   g1_xyzz_t o;
-  o.x = fq_sub(fq_sub(M::mul(r, r), ppp), fq_dbl(q));
-  o.y = fq_sub(M::mul(r, fq_sub(q, o.x)), M::mul(s1, ppp));
-  o.zz = M::mul(M::mul(a.zz, b.zz), pp);
-  o.zzz = M::mul(M::mul(a.zzz, b.zzz), ppp);
+  o.x = fq_sub(fq_sub(rr, ppp), fq_dbl(q));
+  M::mul2(r, fq_sub(q, o.x), s1, ppp, ry, sp);
+  o.y = fq_sub(ry, sp);
+  M::mul2(zz12, pp, zzz12, ppp, o.zz, o.zzz);
   return o;
 }
 

@@ -48,6 +48,15 @@ __device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) {
   return xyzz_add_t<FqTail>(a, b);
 }
 __device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<FqTail>(a); }
+// The same for the kernels that run one warp per SM (the parts' doublings, the last sum):
+// their time is the chain of multiplies, and pairs of independent ones overlap in part
+// (between their carry chains, which share the one carry flag). Where many warps run, the
+// pairs measured slower.
+using FqLat = FqPair;
+__device__ __noinline__ g1_xyzz_t xyzz_add_lat(g1_xyzz_t a, g1_xyzz_t b) {
+  return xyzz_add_t<FqLat>(a, b);
+}
+__device__ __noinline__ g1_xyzz_t xyzz_dbl_lat(g1_xyzz_t a) { return xyzz_dbl_t<FqLat>(a); }
 __device__ __noinline__ g2_xyzz_t g2_add_nl(g2_xyzz_t a, g2_xyzz_t b) {
   return g2_add_t<Fq2Call>(a, b);
 }
@@ -82,6 +91,8 @@ struct G1 {
   static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return xyzz_add(a, b); }
   static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return xyzz_add_nl(a, b); }
   static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return xyzz_dbl_nl(a); }
+  static __device__ __forceinline__ Pt add_lat(const Pt& a, const Pt& b) { return xyzz_add_lat(a, b); }
+  static __device__ __forceinline__ Pt dbl_lat(const Pt& a) { return xyzz_dbl_lat(a); }
   static __device__ __forceinline__ void jacobian(const Pt& p, F* out) {
     xyzz_to_jacobian_t<FqTail>(p, out[0], out[1], out[2]);
   }
@@ -107,6 +118,8 @@ struct G2 {
   static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
   static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
   static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return g2_dbl_nl(a); }
+  static __device__ __forceinline__ Pt add_lat(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
+  static __device__ __forceinline__ Pt dbl_lat(const Pt& a) { return g2_dbl_nl(a); }
   static __device__ __forceinline__ void jacobian(const Pt& p, F* out) { g2_to_jacobian_t<Fq2Call>(p, out); }
   static __device__ __forceinline__ bool canonical(const Aff& a) {
     return fq2_is_canonical(a.x) && fq2_is_canonical(a.y);
@@ -502,14 +515,14 @@ __global__ void __launch_bounds__(32) k_msm_parts(const typename G::Pt* partial,
   const uint32_t lane = threadIdx.x, p = blockIdx.x;
   const uint32_t n_chunks = p < kMsmPairBits ? chunks / 2 : chunks;
   typename G::Pt acc = G::inf();
-  for (uint32_t c = lane; c < n_chunks; c += 32) acc = G::add_nl(acc, partial[p * chunks + c]);
+  for (uint32_t c = lane; c < n_chunks; c += 32) acc = G::add_lat(acc, partial[p * chunks + c]);
   for (uint32_t d = 16; d > 0; d >>= 1) {
     const typename G::Pt o = pt_shfl_down(acc, d);
-    if (lane < d) acc = G::add_nl(acc, o);
+    if (lane < d) acc = G::add_lat(acc, o);
   }
   if (lane == 0) {
     if (p < kMsmPairBits)
-      for (uint32_t k = 0; k <= p; k++) acc = G::dbl_nl(acc);
+      for (uint32_t k = 0; k <= p; k++) acc = G::dbl_lat(acc);
     parts[p] = acc;
   }
 }
@@ -566,7 +579,7 @@ __global__ void __launch_bounds__(32) k_msm_final(const typename G::Pt* parts, t
   typename G::Pt acc = lane <= kMsmSumParts ? parts[lane] : G::inf();
   for (uint32_t d = 8; d > 0; d >>= 1) {
     const typename G::Pt o = pt_shfl_down(acc, d);
-    if (lane < d) acc = G::add_nl(acc, o);
+    if (lane < d) acc = G::add_lat(acc, o);
   }
   if (lane == 0) G::jacobian(acc, out);
 }
