@@ -104,6 +104,12 @@ def measured_peaks():
         return {}
 
 
+def imad_peak():
+    """The derived IMAD peak, results per second: SMs x 32-bit IMAD results per clock per
+    SM x the maximum SM clock (MEASURED_PEAKS.json's, else 2070 MHz)."""
+    return SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+
+
 def plan_for(k):
     """Slice levels of the launch plan (mirrors the library): (kk per level)."""
     if k <= 22:
@@ -136,6 +142,20 @@ def algorithmic_ops(kernel, k, nnz_a, nnz_b):
     if kernel == "join":
         return OPS_PER_MM * n + OPS_PER_FROM_MONT * n
     return 0
+
+
+def h_ops(k, nnz_a, nnz_b):
+    """Algorithmic IMAD results of one whole H on 2^k (the sum of algorithmic_ops over its
+    kernels): 6 (n/2) k + 7n + nnz_A + nnz_B + n multiplies and n reductions."""
+    n = 1 << k
+    return OPS_PER_MM * (3 * n * k + 7 * n + nnz_a + nnz_b + n) + OPS_PER_FROM_MONT * n
+
+
+def hbm_floor_bytes(k, nnz_a, nnz_b, n_wires):
+    """The bytes one H must move at least: the CSR matrices (row pointers, columns, values)
+    and the witness read once, h_mont and h_std written once."""
+    n = 1 << k
+    return 2 * (n + 1) * 4 + (nnz_a + nnz_b) * (4 + 32) + n_wires * 32 + 2 * n * 32
 
 
 class ClockSampler:
@@ -231,6 +251,20 @@ def cpu_baseline(A, B, w, budget_s=12.0, max_runs=20):
     dt = time.perf_counter() - t
     out["msm_points_per_s"] = 512 / dt
     out["msm_sample"] = "512 of the 2^18 bases and scalars (%.2f s), C oracle, one thread" % dt
+    # the other proving-key domains, one thread, median of 5 runs (3 for 2^17); the 2^22
+    # stress H (some 25 s a run on one core) is not timed
+    from bn254_scalar_field_gb300 import synth
+
+    per = {"2^18": out["value"]}
+    for k, reps in ((12, 5), (14, 5), (17, 3)):
+        Ak, Bk, wk = synth.problem(k)
+        ts = []
+        for _ in range(reps):
+            t = time.perf_counter()
+            oracle.compute_h(k, Ak, Bk, wk)
+            ts.append(time.perf_counter() - t)
+        per["2^%d" % k] = 1.0 / statistics.median(ts)
+    out["per_config_h_per_s"] = per
     return out
 
 
@@ -416,6 +450,12 @@ def main():
            "h2d_bytes_per_step": int(w.nbytes), "d2h_bytes_per_step": int(2 * n * 32)}
 
     extra = {"ntt_gelem_s_2^18_in_h": 6 * n / (step_ms / args.steps * 1e-3) / 1e9}
+    # HBM as the secondary roof: the bytes an H must move at least, per step time
+    floor = hbm_floor_bytes(LOG_N, nnz_a, nnz_b, int(w.shape[0]))
+    floor_gbs = floor / (step_ms / args.steps * 1e-3) / 1e9
+    hbm_peak = float(measured_peaks().get("hbm_gbs", 0.0)) or None
+    extra.update({"hbm_floor_bytes_per_h_2^18": floor, "hbm_floor_gb_s_2^18": floor_gbs,
+                  "hbm_floor_frac_of_measured_2^18": floor_gbs / hbm_peak if hbm_peak else None})
     extra.update(batched(torch, dev, ctx, w, n, flush))
     if not args.no_extra and rank == 0:
         extra.update(h_msm(torch, dev, g3h, flush))
@@ -545,7 +585,7 @@ def h_msm(torch, dev, g3h, flush, steps=50, warmup=3):
     ctx.close()
     entries = 16 * n  # nonzero digits: all but about 2^-16 of them
     acc_ms = kt["msm_accumulate"][1] / kt["msm_accumulate"][0]
-    peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    peak = imad_peak()
     achieved = entries * MSM_OPS_PER_MADD / (acc_ms * 1e-3)
     return {"msm_2^18_ms": ms, "msm_2^18_per_s": 1e3 / ms,
             "witness_msm_2^18_ms": wit_ms,
@@ -614,7 +654,7 @@ def g2_msm(torch, dev, g3h, flush, k=16, steps=20):
     wit_ms = statistics.median(a.elapsed_time(b) for a, b in wevs)
     ctx.close()
     acc_ms = kt["msm_accumulate"][1] / kt["msm_accumulate"][0]
-    peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    peak = imad_peak()
     achieved = 16 * n * MSM_G2_OPS_PER_MADD / (acc_ms * 1e-3)
     return {"msm_g2_2^%d_ms" % k: ms,
             "witness_msm_g2_2^%d_ms" % k: wit_ms,
@@ -649,6 +689,8 @@ def other_domains(torch, dev, g3h, synth, flush, steps=200):
         ctx.close()
         out["h_per_s_2^%d" % k] = 1e3 / ms
         out["ms_per_h_2^%d" % k] = ms
+        ops = h_ops(k, int(A[0][-1]), int(B[0][-1]))
+        out["h_2^%d_frac_of_derived_imad_peak" % k] = ops / (ms * 1e-3) / imad_peak()
     return out
 
 
@@ -695,8 +737,8 @@ def stress_2_22(torch, dev, g3h, synth):
     ctx.close()
     peak = float(measured_peaks().get("hbm_gbs", 0.0)) or None
     ops = sum(algorithmic_ops(kn, k, 0, 0) for kn in ("ntt_dif", "ntt_mid", "ntt_dit", "join"))
-    imad_peak = SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
-    return {"h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / imad_peak,
+    peak_imad = imad_peak()
+    return {"h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / peak_imad,
             "ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,
             "h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
             "ntt_gelem_s_2^22_in_h": 6 * n / (h_ms * 1e-3) / 1e9,
