@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -33,6 +34,14 @@ using namespace g3h;
 namespace {
 
 const uint32_t kModulus[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
+
+// The kernels move elements as 16-byte vectors, so a device pointer that is not 16-byte
+// aligned would fault the device; such a call is refused instead (G3H_E_INVAL).
+bool misaligned(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return true;
+  return false;
+}
 
 bool host_canonical(const uint32_t* x) {
   for (int i = 7; i >= 0; i--) {
@@ -784,6 +793,7 @@ int g3h_compute_h(g3h_ctx* c, const uint32_t* witness, uint32_t* h_mont, uint32_
   DeviceGuard guard(c->device);
   const size_t n = c->n;
   fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({witness, h_mont, h_std})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
     return quotient(c, lane0(c), s[0], s[1], s[2], (const fr_t*)witness, (fr_t*)h_mont,
                     (fr_t*)h_std, flags);
@@ -805,6 +815,7 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
   if (!c || !a || !b || !cc || !h_mont || !h_std) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
   const size_t n = c->n;
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({a, b, cc, h_mont, h_std})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
     return quotient(c, lane0(c), (const fr_t*)a, (const fr_t*)b, (const fr_t*)cc, nullptr,
                     (fr_t*)h_mont, (fr_t*)h_std, flags);
@@ -883,6 +894,7 @@ int g3h_compute_h_batch(g3h_ctx* c, uint32_t count, const uint32_t* witnesses,
   if (!h_mont || !h_std || (!witnesses && c->n_wires)) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0u;
+  if (dev && misaligned({witnesses, h_mont, h_std})) return G3H_E_INVAL;
   const uint32_t lanes = std::min(count, kBatchLanes);
   int rc = ensure_lanes(c, lanes, !dev);
   if (rc != G3H_OK) return rc;
@@ -930,6 +942,7 @@ int g3h_gather(g3h_ctx* c, const uint32_t* witness, uint32_t* a, uint32_t* b, ui
   if (!c || !c->has_csr || !a || !b || !cc || (!witness && c->n_wires)) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
   const size_t n = c->n;
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({witness, a, b, cc})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
     return gather(c, (const fr_t*)witness, (fr_t*)a, (fr_t*)b, (fr_t*)cc, flags);
   int rc = ensure_stage(c, (size_t)c->n_wires + 3 * n);
@@ -949,6 +962,7 @@ int g3h_ntt(g3h_ctx* c, uint32_t* data, int inverse, int coset, uint32_t flags) 
   if (!c || !data) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
   const size_t n = c->n;
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({data})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS) return ntt(c, (fr_t*)data, inverse, coset, flags);
   int rc = ensure_stage(c, n);
   if (rc != G3H_OK) return rc;
@@ -970,6 +984,7 @@ int g3h_join(g3h_ctx* c, const uint32_t* ea, const uint32_t* eb, const uint32_t*
       k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(x, y, z, hm, hs, n, check, c->d_err);
     });
   };
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({ea, eb, ec, h_mont, h_std})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
     return launch((const fr_t*)ea, (const fr_t*)eb, (const fr_t*)ec, (fr_t*)h_mont,
                   (fr_t*)h_std);
@@ -997,6 +1012,7 @@ int g3h_mul(g3h_ctx* c, const uint32_t* a, const uint32_t* b, uint32_t* out, siz
       k_mul<<<blocks_for(count, 256), 256, 0, c->stream>>>(x, y, o, count, check, c->d_err);
     });
   };
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({a, b, out})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS) return launch((const fr_t*)a, (const fr_t*)b, (fr_t*)out);
   int rc = ensure_stage(c, 3 * count);
   if (rc != G3H_OK) return rc;
@@ -1021,6 +1037,7 @@ int g3h_mont_to_std(g3h_ctx* c, const uint32_t* in, uint32_t* out, size_t count,
       k_mont_to_std<<<(unsigned)blocks, 256, 0, c->stream>>>(x, o, count, check, c->d_err);
     });
   };
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({in, out})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS) return launch((const fr_t*)in, (fr_t*)out);
   int rc = ensure_stage(c, count);
   if (rc != G3H_OK) return rc;
@@ -1150,6 +1167,7 @@ int msm_prepare(g3h_ctx* c, MsmState& m, const uint32_t* bases, uint32_t n_bases
   using Pt = typename G::Pt;
   using Aff = typename G::Aff;
   if (!c || (!bases && n_bases)) return G3H_E_INVAL;
+  if ((flags & G3H_DEVICE_PTRS) && misaligned({bases})) return G3H_E_INVAL;
   if (n_bases > (1u << G3H_MSM_MAX_LOG)) return G3H_E_RANGE;
   DeviceGuard guard(c->device);
   if (cudaStreamSynchronize(c->stream) != cudaSuccess) return G3H_E_CUDA;
@@ -1210,6 +1228,7 @@ int msm_run(g3h_ctx* c, MsmState& m, const uint32_t* scalars, uint32_t count, ui
   if (count > m.n) return G3H_E_RANGE;
   DeviceGuard guard(c->device);
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0;
+  if (dev && misaligned({scalars, result})) return G3H_E_INVAL;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   if (count == 0) {  // the empty sum: infinity
     if (dev)
@@ -1367,7 +1386,8 @@ int noalloc_launch_ok() { return cudaGetLastError() == cudaSuccess ? G3H_OK : G3
 extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const uint32_t* b,
                                         const uint32_t* c, uint32_t* h_mont, uint32_t* h_std,
                                         void* stream) {
-  if (!a || !b || !c || !h_mont || !h_std) return G3H_E_INVAL;
+  if (!a || !b || !c || !h_mont || !h_std || misaligned({a, b, c, h_mont, h_std}))
+    return G3H_E_INVAL;
   if (log_n > kNoAllocMaxLog) return G3H_E_RANGE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)

@@ -125,6 +125,10 @@ def _ptr(x, device):
     if _is_torch(x):
         if not x.is_contiguous():
             raise ValueError("tensor must be contiguous")
+        if x.element_size() != 4 or x.dtype.is_floating_point or x.dtype.is_complex:
+            raise ValueError("tensors must hold 32-bit integer limbs (int32 or uint32)")
+        if x.is_cuda and x.data_ptr() % 16:
+            raise ValueError("device tensors must start on a 16-byte boundary")
         return ctypes.c_void_p(x.data_ptr()), x.is_cuda
     if not isinstance(x, np.ndarray) or x.dtype != np.uint32 or not x.flags.c_contiguous:
         raise ValueError("host arrays must be C-contiguous numpy uint32")

@@ -32,9 +32,9 @@
  * context's device: the call only enqueues work on the context's stream and returns;
  * g3h_sync waits for it and reports errors found on the device. Device pointers must be
  * 16-byte aligned (elements move as 16-byte vectors; cudaMalloc and torch allocations
- * are). The caller owns every
- * buffer it passes; the context owns its tables, its copy of the CSR matrices and its
- * scratch vectors.
+ * are); a call given one that is not returns G3H_E_INVAL and does nothing. The caller
+ * owns every buffer it passes; the context owns its tables, its copy of the CSR matrices
+ * and its scratch vectors.
  *
  * Errors. Every int-returning call returns G3H_OK (0) or a negative G3H_E_* code; no call
  * aborts or throws. A failed call leaves the context usable. Input elements that are not

@@ -379,6 +379,55 @@ def test_noncanonical_inputs_reported_and_context_survives():
         ctx.mul(x, x, hm, flags=g3h.G3H_NOCHECK)
 
 
+def test_misaligned_device_pointers_refused():
+    """A device pointer off a 16-byte boundary is refused at the C boundary before anything
+    is launched (G3H_E_INVAL; the kernels move 16-byte vectors), and by the binding before
+    the call; a tensor of another element width is refused by the binding."""
+    import ctypes
+
+    torch = _torch()
+    L = g3h.lib()
+    log_n = 6
+    n = 1 << log_n
+    A, B, w = synth.problem(log_n, seed=9)
+    buf = torch.zeros(8 * n + 8, dtype=torch.int32, device="cuda")
+    good = ctypes.c_void_p(buf.data_ptr())
+    off = ctypes.c_void_p(buf.data_ptr() + 4)
+    D, INVAL = g3h.G3H_DEVICE_PTRS, g3h.G3H_E_INVAL
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        h = ctx.handle
+        assert L.g3h_compute_h(h, off, good, good, D) == INVAL
+        assert L.g3h_compute_h(h, good, good, off, D) == INVAL
+        assert L.g3h_compute_h_abc(h, good, good, good, good, off, D) == INVAL
+        assert L.g3h_compute_h_batch(h, 2, off, good, good, D) == INVAL
+        assert L.g3h_gather(h, good, good, off, good, D) == INVAL
+        assert L.g3h_ntt(h, off, 0, 1, D) == INVAL
+        assert L.g3h_join(h, good, off, good, good, good, D) == INVAL
+        assert L.g3h_mul(h, good, good, off, n, D) == INVAL
+        assert L.g3h_mont_to_std(h, off, good, n, D) == INVAL
+        assert L.g3h_msm_prepare(h, off, 4, D) == INVAL
+        assert L.g3h_msm(h, good, 0, off, D) == INVAL
+        assert L.g3h_msm_g2_prepare(h, off, 4, D) == INVAL
+        assert L.g3h_msm_g2(h, off, 0, good, D) == INVAL
+        ctx.sync()
+        assert not buf.any()  # nothing ran
+        # the binding refuses both before the call
+        with pytest.raises(ValueError):
+            ctx.mont_to_std(buf[1:1 + 8 * n], buf[8:8 + 8 * n])
+        with pytest.raises(ValueError):
+            ctx.mont_to_std(buf[:8 * n].view(torch.float32), buf[8:8 + 8 * n])
+        # and the context still computes
+        x = _edge_fr()
+        xd = _dev(x)
+        ctx.mont_to_std(xd, xd)
+        from oracle import fr_int as F
+
+        R = 1 << 256
+        want = [v * pow(R, -1, F.R_MOD) % F.R_MOD for v in F.array_to_ints(x)]
+        assert F.array_to_ints(_host(xd)) == want
+    assert L.g3h_compute_h_abc_static(4, good, good, good, good, off, None) == INVAL
+
+
 def test_domain_only_context_rejects_compute_h():
     with g3h.Context(6) as ctx:
         with pytest.raises(g3h.G3HError) as ei:
