@@ -11,7 +11,8 @@
 // one set of 2^15 buckets for all windows: no per-window bucket sums and no doubling
 // chain between windows. Steps:
 //   0. ones: the bases whose scalar is exactly 1 are summed apart (a tree per block, then
-//      one block), so they do not pile into one bucket;
+//      one block), so they do not pile into one bucket; on a second stream, from the end
+//      of step 3 on;
 //   1. count: per-bucket entry counts of each sort block (one per SM, counters in shared
 //      memory), then per bucket the prefix over the blocks and the total;
 //   2. scan: exclusive prefix sum of the totals (bucket offsets);
