@@ -416,12 +416,18 @@ def main():
     per_h_ops = sum(algorithmic_ops(k, LOG_N, nnz_a, nnz_b) * v[0] for k, v in kt.items())
     per_h_ops /= args.steps
     kernel_ms_sum = sum(v[1] for v in kt.values()) / args.steps
+    # the same pipe measured on this GPU by the library's probe (independent wide
+    # multiply-adds on every SM), outside the timed regions, beside the derived figure
+    measured_tops = ctx.measure_imad() / 1e12
     roofline = {
         "bound": "alu", "kernel": top, "achieved": achieved, "peak": peak_tops,
         "unit": "T IMAD/s", "frac": achieved / peak_tops, "traffic": traffic,
         "peak_source": "derived: %d SMs x %d 32-bit IMAD results/clk/SM x %.0f MHz; a "
                        "32x32->64 product counts two" % (SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
         "whole_step_frac": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / peak_tops,
+        "peak_measured": measured_tops,
+        "frac_of_measured": achieved / measured_tops,
+        "whole_step_frac_of_measured": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / measured_tops,
         "timing": "step times from a pass without per-kernel events (vectors on three "
                   "streams); kernel times from a second pass of the same K steps with the "
                   "library's per-launch events and the three vectors in one launch per "

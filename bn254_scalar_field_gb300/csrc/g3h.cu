@@ -1343,6 +1343,80 @@ int g3h_timing_read(g3h_ctx* c, g3h_kernel_time* out, int max, int* count) {
 
 }  // extern "C"
 
+namespace g3h {
+
+// Throughput probe of the integer multiply pipe, for the roofline's denominator (32-bit
+// IMAD results per second): eight independent chains of 32-bit multiply-adds
+// (mad.lo.u32, y <- y * c + a) per thread, sixteen per chain and loop iteration; every
+// product takes the chain's value so far, so none can be computed once and reused.
+// Nothing is read; sink[0] is written only if the chains' final values XOR to `seed`,
+// which keeps them live. Launch: any grid of 256 threads.
+__global__ void __launch_bounds__(256) k_imad_probe(uint32_t* sink, uint32_t iters, uint32_t seed) {
+  uint32_t y[8], a[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    a[k] = seed * (threadIdx.x + 1u) + (uint32_t)k * 0x9e3779b9u;
+    y[k] = a[k];
+  }
+  const uint32_t c = seed ^ (blockIdx.x * 0x85ebca6bu);
+  for (uint32_t it = 0; it < iters; it++) {
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+#pragma unroll
+      for (int k = 0; k < 8; k++)
+        asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(y[k]) : "r"(c ^ a[k]), "r"(a[k]));
+    }
+  }
+  uint32_t s = 0;
+#pragma unroll
+  for (int k = 0; k < 8; k++) s ^= y[k];
+  if (s == seed) sink[0] = s;
+}
+
+}  // namespace g3h
+
+extern "C" {
+
+int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
+  if (!c || !results_per_s) return G3H_E_INVAL;
+  DeviceGuard guard(c->device);
+  uint32_t* sink = nullptr;
+  if (cudaMalloc((void**)&sink, sizeof(uint32_t)) != cudaSuccess) return G3H_E_NOMEM;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int rc = cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess
+               ? G3H_OK
+               : G3H_E_CUDA;
+  // four blocks of eight warps per SM; about 4 ms a run at 2 x 10^13 results per second
+  const unsigned grid = (unsigned)c->sm_count * 4;
+  const uint32_t iters = 4096;
+  double best = 0.0;
+  for (int run = 0; run < 4 && rc == G3H_OK; run++) {
+    const uint32_t it = run == 0 ? 64u : iters;  // the first run warms up
+    k_imad_probe<<<grid, 256, 0, c->stream>>>(sink, it, 0x2545f491u + (uint32_t)run);
+    if (cudaGetLastError() != cudaSuccess) rc = G3H_E_CUDA;
+    if (run == 0 || rc != G3H_OK) continue;
+    cudaEventRecord(e0, c->stream);
+    k_imad_probe<<<grid, 256, 0, c->stream>>>(sink, it, 0x9e3779b1u + (uint32_t)run);
+    cudaEventRecord(e1, c->stream);
+    float ms = 0.f;
+    if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.f) {
+      rc = G3H_E_CUDA;
+      continue;
+    }
+    const double results = (double)grid * 256.0 * it * 16.0 * 8.0;
+    best = std::max(best, results / (ms * 1e-3));
+  }
+  if (rc == G3H_OK && cudaStreamSynchronize(c->stream) != cudaSuccess) rc = G3H_E_CUDA;
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaFree(sink);
+  if (rc == G3H_OK) *results_per_s = best;
+  return rc;
+}
+
+}  // extern "C"
+
 // ---------------------------------------------------------------------------------------
 // g3h_compute_h_abc_static: steps 2-5 without any allocation.
 //

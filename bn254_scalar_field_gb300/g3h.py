@@ -40,7 +40,7 @@ ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
                 "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
                 "g3h_compute_h_batch", "g3h_mont_to_std", "g3h_msm_prepare", "g3h_msm",
-                "g3h_msm_g2_prepare", "g3h_msm_g2")
+                "g3h_msm_g2_prepare", "g3h_msm_g2", "g3h_measure_imad")
 
 
 class G3HError(RuntimeError):
@@ -95,6 +95,7 @@ def lib():
                                       ctypes.POINTER(I)]
         L.g3h_compute_h_abc_static.argtypes = [U, P, P, P, P, P, P]
         L.g3h_compute_h_batch.argtypes = [P, U, P, P, P, U]
+        L.g3h_measure_imad.argtypes = [P, ctypes.POINTER(ctypes.c_double)]
         for name in ENTRY_POINTS:
             if name not in ("g3h_destroy", "g3h_strerror"):
                 getattr(L, name).restype = ctypes.c_int
@@ -283,6 +284,13 @@ def g3h_msm_g2(ctx, scalars, result, flags=0):
     _check(lib().g3h_msm_g2(ctx, bufs[0][0], _elems(scalars), bufs[1][0], f), "g3h_msm_g2")
 
 
+def g3h_measure_imad(ctx):
+    """The device's measured 32-bit IMAD results per second (the roofline's unit)."""
+    v = ctypes.c_double()
+    _check(lib().g3h_measure_imad(ctx, ctypes.byref(v)), "g3h_measure_imad")
+    return v.value
+
+
 def g3h_sync(ctx):
     _check(lib().g3h_sync(ctx), "g3h_sync")
 
@@ -375,6 +383,9 @@ class Context:
 
     def msm_g2(self, scalars, result, flags=0):
         g3h_msm_g2(self.handle, scalars, result, flags)
+
+    def measure_imad(self):
+        return g3h_measure_imad(self.handle)
 
     def sync(self):
         g3h_sync(self.handle)

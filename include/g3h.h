@@ -264,6 +264,13 @@ typedef struct {
 } g3h_kernel_time;
 int g3h_timing_read(g3h_ctx* ctx, g3h_kernel_time* out, int max, int* count);
 
+/* For measurement: the throughput of the device's integer multiply pipe in the unit of
+ * the library's roofline, 32-bit IMAD results per second. A probe kernel runs independent
+ * chains of 32-bit multiply-adds (mad.lo.u32) on every SM for a few milliseconds, timed
+ * with CUDA events on the context's stream (best of three runs after a warm-up).
+ * Synchronous. Returns G3H_E_INVAL (NULL), G3H_E_NOMEM or G3H_E_CUDA. */
+int g3h_measure_imad(g3h_ctx* ctx, double* results_per_s);
+
 #ifdef __cplusplus
 }
 #endif

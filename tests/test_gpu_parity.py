@@ -428,6 +428,15 @@ def test_misaligned_device_pointers_refused():
     assert L.g3h_compute_h_abc_static(4, good, good, good, good, off, None) == INVAL
 
 
+def test_measure_imad_probe():
+    """The multiply-pipe probe returns a rate close to the derived peak (152 SMs x 64 32-bit
+    IMAD results per clock at up to 2.07 GHz), its unit being the roofline's."""
+    with g3h.Context(4) as ctx:
+        rate = ctx.measure_imad()
+    derived = 152 * 64 * 2.07e9
+    assert 0.5 * derived < rate < 1.1 * derived
+
+
 def test_domain_only_context_rejects_compute_h():
     with g3h.Context(6) as ctx:
         with pytest.raises(g3h.G3HError) as ei:
