@@ -48,20 +48,173 @@ using FqTail = FqCall;
 __device__ __noinline__ g1_xyzz_t xyzz_add_nl(g1_xyzz_t a, g1_xyzz_t b) {
   return xyzz_add_t<FqTail>(a, b);
 }
-__device__ __noinline__ g1_xyzz_t xyzz_dbl_nl(g1_xyzz_t a) { return xyzz_dbl_t<FqTail>(a); }
-// The same for the kernels that run one warp per SM (the parts' doublings, the last sum):
-// their time is the chain of multiplies, and pairs of independent ones overlap in part
-// (between their carry chains, which share the one carry flag). Where many warps run, the
-// pairs measured slower.
+// The same for the kernels that run one warp per SM (the upper levels of the parts' and
+// the last sum's trees): their time is the chain of multiplies, and pairs of independent
+// ones overlap in part (between their carry chains, which share the one carry flag).
+// Where many warps run, the pairs measured slower.
 using FqLat = FqPair;
 __device__ __noinline__ g1_xyzz_t xyzz_add_lat(g1_xyzz_t a, g1_xyzz_t b) {
   return xyzz_add_t<FqLat>(a, b);
 }
-__device__ __noinline__ g1_xyzz_t xyzz_dbl_lat(g1_xyzz_t a) { return xyzz_dbl_t<FqLat>(a); }
 __device__ __noinline__ g2_xyzz_t g2_add_nl(g2_xyzz_t a, g2_xyzz_t b) {
   return g2_add_t<Fq2Call>(a, b);
 }
-__device__ __noinline__ g2_xyzz_t g2_dbl_nl(g2_xyzz_t a) { return g2_dbl_t<Fq2Call>(a); }
+
+// Doublings by a whole warp, for the one-lane chain of doublings in the parts' kernel:
+// every lane holds the point, the independent F_q products of each step of dbl-2008-s-1
+// go to different lanes (one out-of-line multiply each) and come back by shuffles, so a
+// doubling waits on four multiplies instead of nine (G1) or 27 (G2). The products and
+// their operands are those of xyzz_dbl_t / g2_dbl_t, so the results are the same
+// representatives. All 32 lanes must call it together.
+__device__ __forceinline__ fq_t fq_shfl(const fq_t& x, uint32_t src) {
+  fq_t o;
+#pragma unroll
+  for (int i = 0; i < 8; i++) o.v[i] = __shfl_sync(0xffffffffu, x.v[i], src);
+  return o;
+}
+
+__device__ __forceinline__ fq_t fq_sel(bool c, const fq_t& a, const fq_t& b) {
+  fq_t o;
+#pragma unroll
+  for (int i = 0; i < 8; i++) o.v[i] = c ? a.v[i] : b.v[i];
+  return o;
+}
+
+
+
+__device__ __noinline__ g1_xyzz_t xyzz_dbl_coop(g1_xyzz_t p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const fq_t u = fq_dbl(p.y);
+  // V = U U (lane 0), XX = X X (lane 1)
+  const fq_t a1 = fq_sel(lane == 0, u, p.x);
+  fq_t r = fq_mul_call(a1, a1);
+  const fq_t v = fq_shfl(r, 0), xx = fq_shfl(r, 1);
+  // W = U V (0), S = X V (1), ZZ3 = ZZ V (2; the Montgomery product is symmetric)
+  r = fq_mul_call(fq_sel(lane == 0, u, fq_sel(lane == 1, p.x, p.zz)), v);
+  const fq_t w = fq_shfl(r, 0), s = fq_shfl(r, 1), zz3 = fq_shfl(r, 2);
+  const fq_t m = fq_add(fq_dbl(xx), xx);
+  // M M (0), W Y (1), W ZZZ (2)
+  r = fq_mul_call(fq_sel(lane == 0, m, w), fq_sel(lane == 0, m, fq_sel(lane == 1, p.y, p.zzz)));
+  const fq_t mm = fq_shfl(r, 0), wy = fq_shfl(r, 1), zzz3 = fq_shfl(r, 2);
+  g1_xyzz_t o;
+  o.x = fq_sub(mm, fq_dbl(s));
+  o.y = fq_sub(fq_mul_call(m, fq_sub(s, o.x)), wy);
+  o.zz = zz3;
+  o.zzz = zzz3;
+  return o;
+}
+
+// The F_q products of an F_q2 product a b (Karatsuba, as fq2_mul_t): k = 0: a0 b0,
+// 1: a1 b1, 2: (a0 + a1)(b0 + b1); and of a square (as fq2_sqr_t): 0: a0 a1,
+// 1: (a0 + a1)(a0 - a1).
+__device__ __forceinline__ void fq2_mul_operands(uint32_t k, const fq2_t& a, const fq2_t& b,
+                                                 fq_t& x, fq_t& y) {
+  x = k == 0 ? a.c0 : (k == 1 ? a.c1 : fq_add(a.c0, a.c1));
+  y = k == 0 ? b.c0 : (k == 1 ? b.c1 : fq_add(b.c0, b.c1));
+}
+__device__ __forceinline__ void fq2_sqr_operands(uint32_t k, const fq2_t& a, fq_t& x, fq_t& y) {
+  x = k == 0 ? a.c0 : fq_add(a.c0, a.c1);
+  y = k == 0 ? a.c1 : fq_sub(a.c0, a.c1);
+}
+// The F_q2 product from its three F_q products on lanes l, l + 1, l + 2.
+__device__ __forceinline__ fq2_t fq2_mul_gather(const fq_t& r, uint32_t l) {
+  const fq_t v0 = fq_shfl(r, l), v1 = fq_shfl(r, l + 1), sm = fq_shfl(r, l + 2);
+  return {fq_sub(v0, v1), fq_sub(fq_sub(sm, v0), v1)};
+}
+// The F_q2 square from its two F_q products on lanes l, l + 1.
+__device__ __forceinline__ fq2_t fq2_sqr_gather(const fq_t& r, uint32_t l) {
+  const fq_t t = fq_shfl(r, l), c0 = fq_shfl(r, l + 1);
+  return {c0, fq_dbl(t)};
+}
+
+__device__ __noinline__ g2_xyzz_t g2_dbl_coop(g2_xyzz_t p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  fq_t x, y;
+  const fq2_t u = fq2_dbl(p.y);
+  // V = U^2 (lanes 0-1), XX = X^2 (lanes 2-3)
+  fq2_sqr_operands(lane & 1u, lane < 2 ? u : p.x, x, y);
+  fq_t r = fq_mul_call(x, y);
+  const fq2_t v = fq2_sqr_gather(r, 0), xx = fq2_sqr_gather(r, 2);
+  // W = U V (0-2), S = X V (3-5), ZZ3 = V ZZ (6-8)
+  {
+    const uint32_t g = lane < 3 ? 0u : (lane < 6 ? 1u : 2u);
+    const fq2_t a = g == 0 ? u : (g == 1 ? p.x : v);
+    const fq2_t b = g == 2 ? p.zz : v;
+    fq2_mul_operands(lane - 3u * g, a, b, x, y);
+  }
+  r = fq_mul_call(x, y);
+  const fq2_t w = fq2_mul_gather(r, 0), s = fq2_mul_gather(r, 3), zz3 = fq2_mul_gather(r, 6);
+  const fq2_t m = fq2_add(fq2_dbl(xx), xx);
+  // M^2 (0-1), W Y (2-4), W ZZZ (5-7)
+  if (lane < 2) {
+    fq2_sqr_operands(lane, m, x, y);
+  } else {
+    const uint32_t g = lane < 5 ? 0u : 1u;
+    fq2_mul_operands(lane - 2u - 3u * g, w, g == 0 ? p.y : p.zzz, x, y);
+  }
+  r = fq_mul_call(x, y);
+  const fq2_t mm = fq2_sqr_gather(r, 0), wy = fq2_mul_gather(r, 2), zzz3 = fq2_mul_gather(r, 5);
+  g2_xyzz_t o;
+  o.x = fq2_sub(mm, fq2_dbl(s));
+  // M (S - X3) (0-2)
+  fq2_mul_operands(lane < 3 ? lane : 2u, m, fq2_sub(s, o.x), x, y);
+  r = fq_mul_call(x, y);
+  o.y = fq2_sub(fq2_mul_gather(r, 0), wy);
+  o.zz = zz3;
+  o.zzz = zzz3;
+  return o;
+}
+
+// An addition by a whole warp (add-2008-s, as xyzz_add_t, the same products of the same
+// operands): four steps of independent F_q products spread over the lanes. Every lane
+// passes the same a and b; all 32 lanes must call it together. (Over G2 the same scheme,
+// 18 lanes per step, measured slower than one thread per addition: 1.63 -> 1.65 ms.)
+__device__ __noinline__ g1_xyzz_t xyzz_add_coop(g1_xyzz_t a, g1_xyzz_t b) {
+  if (xyzz_is_inf(a)) return b;
+  if (xyzz_is_inf(b)) return a;
+  const uint32_t lane = threadIdx.x & 31u;
+  // U1 = X1 ZZ2 (0), U2 = X2 ZZ1 (1), S1 = Y1 ZZZ2 (2), S2 = Y2 ZZZ1 (3), ZZ1 ZZ2 (4),
+  // ZZZ1 ZZZ2 (5)
+  const fq_t x = fq_sel(lane == 0, a.x, fq_sel(lane == 1, b.x, fq_sel(lane == 2, a.y,
+                 fq_sel(lane == 3, b.y, fq_sel(lane == 4, a.zz, a.zzz)))));
+  const fq_t y = fq_sel(lane == 0, b.zz, fq_sel(lane == 1, a.zz, fq_sel(lane == 2, b.zzz,
+                 fq_sel(lane == 3, a.zzz, fq_sel(lane == 4, b.zz, b.zzz)))));
+  fq_t r = fq_mul_call(x, y);
+  const fq_t u1 = fq_shfl(r, 0), u2 = fq_shfl(r, 1), s1 = fq_shfl(r, 2), s2 = fq_shfl(r, 3);
+  const fq_t zz12 = fq_shfl(r, 4), zzz12 = fq_shfl(r, 5);
+  const fq_t p = fq_sub(u2, u1), rr0 = fq_sub(s2, s1);
+  if (fq_is_zero(p)) {
+    if (fq_is_zero(rr0)) return xyzz_dbl_coop(a);
+    return xyzz_infinity();
+  }
+  // PP = P P (0), RR = R R (1)
+  const fq_t pr = fq_sel(lane == 0, p, rr0);
+  r = fq_mul_call(pr, pr);
+  const fq_t pp = fq_shfl(r, 0), rr = fq_shfl(r, 1);
+  // PPP = P PP (0), Q = U1 PP (1), ZZ3 = ZZ1 ZZ2 PP (2)
+  r = fq_mul_call(fq_sel(lane == 0, p, fq_sel(lane == 1, u1, zz12)), pp);
+  const fq_t ppp = fq_shfl(r, 0), q = fq_shfl(r, 1);
+  g1_xyzz_t o;
+  o.zz = fq_shfl(r, 2);
+  o.x = fq_sub(fq_sub(rr, ppp), fq_dbl(q));
+  // R (Q - X3) (0), S1 PPP (1), ZZZ1 ZZZ2 PPP (2)
+  r = fq_mul_call(fq_sel(lane == 0, rr0, fq_sel(lane == 1, s1, zzz12)),
+                  fq_sel(lane == 0, fq_sub(q, o.x), ppp));
+  o.y = fq_sub(fq_shfl(r, 0), fq_shfl(r, 1));
+  o.zzz = fq_shfl(r, 2);
+  return o;
+}
+
+// One level of a shuffle tree by the whole warp: lanes j < d replace acc by acc + o, one
+// addition after another, each by all lanes. All 32 lanes must call it together.
+template <class G>
+__device__ __forceinline__ void coop_level(typename G::Pt& acc, const typename G::Pt& o, uint32_t d) {
+  const uint32_t lane = threadIdx.x & 31u;
+  for (uint32_t j = 0; j < d; j++) {
+    const typename G::Pt r = G::add_coop(pt_shfl(acc, j), pt_shfl(o, j));
+    if (lane == j) acc = r;
+  }
+}
 
 template <class P>
 __device__ __forceinline__ P pt_shfl_down(const P& p, uint32_t d) {
@@ -71,6 +224,17 @@ __device__ __forceinline__ P pt_shfl_down(const P& p, uint32_t d) {
   uint32_t* dst = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
   for (int w = 0; w < words; w++) dst[w] = __shfl_down_sync(0xffffffffu, src[w], d);
+  return o;
+}
+
+template <class P>
+__device__ __forceinline__ P pt_shfl(const P& p, uint32_t src) {
+  constexpr int words = sizeof(P) / 4;
+  const uint32_t* in = reinterpret_cast<const uint32_t*>(&p);
+  P o;
+  uint32_t* out = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int w = 0; w < words; w++) out[w] = __shfl_sync(0xffffffffu, in[w], src);
   return o;
 }
 
@@ -91,9 +255,12 @@ struct G1 {
   static __device__ __forceinline__ Pt madd(const Pt& acc, const Aff& a) { return xyzz_madd(acc, a); }
   static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return xyzz_add(a, b); }
   static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return xyzz_add_nl(a, b); }
-  static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return xyzz_dbl_nl(a); }
   static __device__ __forceinline__ Pt add_lat(const Pt& a, const Pt& b) { return xyzz_add_lat(a, b); }
-  static __device__ __forceinline__ Pt dbl_lat(const Pt& a) { return xyzz_dbl_lat(a); }
+  static __device__ __forceinline__ Pt dbl_coop(const Pt& a) { return xyzz_dbl_coop(a); }
+  static __device__ __forceinline__ Pt add_coop(const Pt& a, const Pt& b) { return xyzz_add_coop(a, b); }
+  // the one-warp trees' levels of at most this many additions go to coop_level (1 and 2
+  // measured best: parts and last sum 111 -> 102 us)
+  static constexpr uint32_t kCoopLevels = 2;
   static __device__ __forceinline__ void jacobian(const Pt& p, F* out) {
     xyzz_to_jacobian_t<FqTail>(p, out[0], out[1], out[2]);
   }
@@ -118,9 +285,9 @@ struct G2 {
   static __device__ __forceinline__ Pt madd(const Pt& acc, const Aff& a) { return g2_madd_t<Fq2Call>(acc, a); }
   static __device__ __forceinline__ Pt add(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
   static __device__ __forceinline__ Pt add_nl(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
-  static __device__ __forceinline__ Pt dbl_nl(const Pt& a) { return g2_dbl_nl(a); }
   static __device__ __forceinline__ Pt add_lat(const Pt& a, const Pt& b) { return g2_add_nl(a, b); }
-  static __device__ __forceinline__ Pt dbl_lat(const Pt& a) { return g2_dbl_nl(a); }
+  static __device__ __forceinline__ Pt dbl_coop(const Pt& a) { return g2_dbl_coop(a); }
+  static constexpr uint32_t kCoopLevels = 0;
   static __device__ __forceinline__ void jacobian(const Pt& p, F* out) { g2_to_jacobian_t<Fq2Call>(p, out); }
   static __device__ __forceinline__ bool canonical(const Aff& a) {
     return fq2_is_canonical(a.x) && fq2_is_canonical(a.y);
@@ -449,7 +616,8 @@ __global__ void __launch_bounds__(G::kTree) k_msm_merge_long(const uint32_t* off
 //   Q = sum_t (V_t + 2t U_t) = sum_t V_t + sum_{b < 14} 2^(b+1) sum_{t : bit b of t} U_t.
 // Part p < 14 is the sum over U_t with bit p of t set; part 14 is the sum of V. The point
 // operations of steps 6-9 are a chain of some thirty dependent ones on few warps: their
-// time is latency, and they use the out-of-line copies (add_nl, dbl_nl).
+// time is latency, and they use the out-of-line copies (add_nl, add_lat) and, where one
+// warp works on one point, the warp-cooperative dbl_coop and add_coop.
 constexpr uint32_t kMsmPairs = kMsmBuckets / 2;          // 16384 = 2^14
 constexpr uint32_t kMsmPairBits = 14;
 constexpr uint32_t kMsmSumParts = kMsmPairBits + 1;      // 15
@@ -519,13 +687,21 @@ __global__ void __launch_bounds__(32) k_msm_parts(const typename G::Pt* partial,
   for (uint32_t c = lane; c < n_chunks; c += 32) acc = G::add_lat(acc, partial[p * chunks + c]);
   for (uint32_t d = 16; d > 0; d >>= 1) {
     const typename G::Pt o = pt_shfl_down(acc, d);
+    if constexpr (G::kCoopLevels > 0) {
+      if (d <= G::kCoopLevels) {
+        coop_level<G>(acc, o, d);
+        continue;
+      }
+    }
     if (lane < d) acc = G::add_lat(acc, o);
   }
-  if (lane == 0) {
-    if (p < kMsmPairBits)
-      for (uint32_t k = 0; k <= p; k++) acc = G::dbl_lat(acc);
-    parts[p] = acc;
+  // the doublings by the whole warp, on lane 0's sum (106 -> 72 us for G1; G2 multiexp
+  // 1.75 -> 1.63 ms)
+  if (p < kMsmPairBits) {
+    acc = pt_shfl(acc, 0u);
+    for (uint32_t k = 0; k <= p; k++) acc = G::dbl_coop(acc);
   }
+  if (lane == 0) parts[p] = acc;
 }
 
 // The sum of the bases whose scalar is 1, beside the bucket path: each thread adds its
@@ -580,6 +756,12 @@ __global__ void __launch_bounds__(32) k_msm_final(const typename G::Pt* parts, t
   typename G::Pt acc = lane <= kMsmSumParts ? parts[lane] : G::inf();
   for (uint32_t d = 8; d > 0; d >>= 1) {
     const typename G::Pt o = pt_shfl_down(acc, d);
+    if constexpr (G::kCoopLevels > 0) {
+      if (d <= G::kCoopLevels) {
+        coop_level<G>(acc, o, d);
+        continue;
+      }
+    }
     if (lane < d) acc = G::add_lat(acc, o);
   }
   if (lane == 0) G::jacobian(acc, out);
