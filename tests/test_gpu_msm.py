@@ -8,8 +8,9 @@ Cases: ragged sizes (1 .. 4099 bases, fewer scalars than bases, none), host and 
 buffers, scalars at the digit boundaries (2^15, 2^15 + 1, 2^16 - 1 in a window: the
 signed-digit carry), 0, 1, r - 1, one scalar for every base (all entries in a few
 buckets: the slices' load balance), witness scalars (mostly 0 and 1), equal bases with equal scalars (the doubling case of
-the mixed addition), P and -P (cancellation), bases at infinity, the chain from
-g3h_compute_h's h_std, the full 2^18 workload, and the input checks.
+the mixed addition), P and -P (cancellation), bases at infinity, equal and opposite
+sums meeting in the bucket sum's last additions, the chain from g3h_compute_h's h_std,
+the full 2^18 workload, and the input checks.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -154,6 +155,21 @@ def test_msm_exceptional_additions():
     s2 = np.repeat(synth_g1.scalars(1, seed=17), 16, axis=0)
     got = _run(pts2, s2)
     assert not got.any() and not oracle.g1_msm(pts2, s2).any()
+
+
+def test_msm_tail_equal_and_opposite_sums():
+    """The bucket sum's last additions on equal or opposite points (the exceptional cases
+    of the whole-warp addition): P with scalar 2 makes the V part 2P, and two bases with
+    scalar 1 make the ones' sum 2P or -2P, so the final sum adds 2P to 2P (a doubling) or
+    to -2P (infinity)."""
+    base = synth_g1.points(2, seed=15)  # base[1] = -base[0]
+    two, one = F.ints_to_array([2]), F.ints_to_array([1])
+    for second, cancels in ((base[:1], False), (base[1:2], True)):
+        pts = np.concatenate([base[:1], second, second])
+        s = np.concatenate([two, one, one])
+        want = oracle.g1_msm(pts, s)
+        assert np.array_equal(_run(pts, s), want)
+        assert (not want.any()) == cancels
 
 
 def test_msm_on_h_std():
