@@ -80,8 +80,6 @@ __device__ __forceinline__ fq_t fq_sel(bool c, const fq_t& a, const fq_t& b) {
   return o;
 }
 
-
-
 __device__ __noinline__ g1_xyzz_t xyzz_dbl_coop(g1_xyzz_t p) {
   const uint32_t lane = threadIdx.x & 31u;
   const fq_t u = fq_dbl(p.y);
