@@ -37,7 +37,6 @@ WORKLOAD = "groth16_h_bn254_2^18"
 # word) and 8 low-only products; a Montgomery reduction (from_mont) 64 full and 8 low.
 OPS_PER_MM = 2 * 128 + 8
 OPS_PER_FROM_MONT = 2 * 64 + 8
-SM_COUNT = 152
 IMAD_PER_CLK_PER_SM = 64  # 32-bit integer multiply-add results per clock per SM
 L2_FLUSH_BYTES = 256 << 20
 
@@ -104,10 +103,23 @@ def measured_peaks():
         return {}
 
 
+_SM_COUNT = None
+
+
+def sm_count():
+    """The device's SM count (cudaDevAttrMultiProcessorCount, through torch)."""
+    global _SM_COUNT
+    if _SM_COUNT is None:
+        import torch
+
+        _SM_COUNT = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return _SM_COUNT
+
+
 def imad_peak():
     """The derived IMAD peak, results per second: SMs x 32-bit IMAD results per clock per
     SM x the maximum SM clock (MEASURED_PEAKS.json's, else 2070 MHz)."""
-    return SM_COUNT * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
+    return sm_count() * IMAD_PER_CLK_PER_SM * float(measured_peaks().get("sm_max_mhz", 2070.0)) * 1e6
 
 
 def plan_for(k):
@@ -121,34 +133,62 @@ def plan_for(k):
     return [lo, mid, rest - mid]
 
 
-def algorithmic_ops(kernel, k, nnz_a, nnz_b):
-    """Algorithmic 32-bit IMAD results of one launch, from the method's multiply count per
-    H: 6 (n/2) k butterfly multiplies, 3n for 1/n, 3n for the shift, n for the join
-    product, nnz_A + nnz_B + n for the gather, and n Montgomery reductions for h_std."""
+def kernel_counts_per_h(k, nnz_a, nnz_b, from_witness=True):
+    """The method's Montgomery multiplies and reductions (from_mont) of one whole H on 2^k
+    (SURVEY's count), charged to the kernel that does them, as {name: (multiplies,
+    reductions)}. gather_a / gather_b: one multiply per term of A / of B; ntt_dif: the
+    butterflies of the inverse's top slice levels (3 vectors) and, from a witness, the n
+    products c = a * b formed at its load; ntt_mid: the low levels of both transforms, the
+    1/n scale and the coset shift (3 vectors); ntt_dit: the forward's top levels; join: n
+    products a * b and the n reductions of h_std."""
     n = 1 << k
     kk = plan_for(k)
-    if kernel == "gather":
-        return OPS_PER_MM * (nnz_a + nnz_b + n)
-    if kernel == "ntt_dif":
-        return OPS_PER_MM * 3 * kk[-1] * (n // 2)
-    if kernel == "ntt_dif_gather":
-        return OPS_PER_MM * (3 * kk[-1] * (n // 2) + nnz_a + nnz_b + n)
-    if kernel == "ntt_mid":
-        return OPS_PER_MM * 3 * (kk[0] * n + 2 * n)
-    if kernel == "ntt_dit_join":
-        return OPS_PER_MM * (3 * kk[-1] * (n // 2) + n) + OPS_PER_FROM_MONT * n
-    if kernel == "ntt_dit":
-        return OPS_PER_MM * 3 * kk[-1] * (n // 2)
-    if kernel == "join":
-        return OPS_PER_MM * n + OPS_PER_FROM_MONT * n
-    return 0
+    top = sum(kk[1:])
+    c = {}
+    if from_witness:
+        c["gather_a"] = (nnz_a, 0)
+        c["gather_b"] = (nnz_b, 0)
+    c["ntt_dif"] = (3 * top * (n // 2) + (n if from_witness else 0), 0)
+    c["ntt_mid"] = (3 * (kk[0] * n + 2 * n), 0)
+    c["ntt_dit"] = (3 * top * (n // 2), 0)
+    c["join"] = (n, n)
+    return c
 
 
-def h_ops(k, nnz_a, nnz_b):
-    """Algorithmic IMAD results of one whole H on 2^k (the sum of algorithmic_ops over its
-    kernels): 6 (n/2) k + 7n + nnz_A + nnz_B + n multiplies and n reductions."""
+def kernel_ops_per_h(k, nnz_a, nnz_b, from_witness=True, mm_ops=None, red_ops=None):
+    """Algorithmic 32-bit IMAD results of one whole H per kernel name: the counts above at
+    mm_ops per multiply and red_ops per reduction (default: 264 and 136, a full 32 x 32
+    product counted as two results). Their sum is h_ops."""
+    mm_ops = OPS_PER_MM if mm_ops is None else mm_ops
+    red_ops = OPS_PER_FROM_MONT if red_ops is None else red_ops
+    return {name: mm * mm_ops + red * red_ops
+            for name, (mm, red) in kernel_counts_per_h(k, nnz_a, nnz_b, from_witness).items()}
+
+
+def launches_per_h(k, from_witness=True):
+    """Launches per kernel name of one H with G3H_SERIALIZE (three vectors per launch)."""
+    levels = len(plan_for(k))
+    out = {"ntt_dif": levels - 1, "ntt_mid": 1, "ntt_dit": levels - 1, "join": 1}
+    if from_witness:
+        out.update({"gather_a": 1, "gather_b": 1})
+    return out
+
+
+def algorithmic_ops(kernel, k, nnz_a, nnz_b, from_witness=True):
+    """Algorithmic 32-bit IMAD results of one launch of `kernel` (serialized H)."""
+    ops = kernel_ops_per_h(k, nnz_a, nnz_b, from_witness)
+    if kernel not in ops:
+        return 0
+    return ops[kernel] // launches_per_h(k, from_witness)[kernel]
+
+
+def h_ops(k, nnz_a, nnz_b, from_witness=True):
+    """Algorithmic IMAD results of one whole H on 2^k, SURVEY's count: 6 (n/2) k + 7n
+    multiplies (butterflies, 1/n, shift, join), with a witness nnz_A + nnz_B + n more (the
+    gather and c = a * b), and n reductions."""
     n = 1 << k
-    return OPS_PER_MM * (3 * n * k + 7 * n + nnz_a + nnz_b + n) + OPS_PER_FROM_MONT * n
+    mm = 3 * n * k + 7 * n + ((nnz_a + nnz_b + n) if from_witness else 0)
+    return OPS_PER_MM * mm + OPS_PER_FROM_MONT * n
 
 
 def hbm_floor_bytes(k, nnz_a, nnz_b, n_wires):
@@ -393,16 +433,20 @@ def main():
     launches = args.steps * sum(v[0] for v in ctx.timing_read().values())
     ctx.timing_enable(False)
 
-    # roofline of the dominant kernel: algorithmic IMAD-class ops per launch / mean time
+    # roofline of the dominant kernel: algorithmic IMAD results per launch / mean time
     top = max(kt, key=lambda k: kt[k][1])
     top_launches, top_ms = kt[top]
     per_launch_ms = top_ms / top_launches
+    per_h = launches_per_h(LOG_N)
+    census = {k: v[0] / args.steps for k, v in kt.items()}
     ops = algorithmic_ops(top, LOG_N, nnz_a, nnz_b)
     peaks = measured_peaks()
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    peak_tops = SM_COUNT * IMAD_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+    sms = sm_count()
+    peak_tops = sms * IMAD_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
     achieved = ops / (per_launch_ms * 1e-3) / 1e12
     traffic = None
+    heavy_pct = None
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             rec = json.load(f)
@@ -411,23 +455,45 @@ def main():
         ent = rec.get(top)
         if ent and ent.get("kernel_digest") == kernel_digest(top) and ent.get("log_n") == LOG_N:
             traffic = ent["bytes_per_launch"]
+            heavy_pct = ent.get("pipe_fma_heavy_pct")
     except (OSError, ValueError, ImportError):
         pass
-    per_h_ops = sum(algorithmic_ops(k, LOG_N, nnz_a, nnz_b) * v[0] for k, v in kt.items())
-    per_h_ops /= args.steps
+    per_h_ops = h_ops(LOG_N, nnz_a, nnz_b)
+    step_s_1 = step_ms / args.steps * 1e-3
     kernel_ms_sum = sum(v[1] for v in kt.values()) / args.steps
-    # the same pipe measured on this GPU by the library's probe (independent wide
-    # multiply-adds on every SM), outside the timed regions, beside the derived figure
-    measured_tops = ctx.measure_imad() / 1e12
+    # the multiply pipe measured on this GPU by the library's probes (independent chains of
+    # mad.lo, mad.hi and mad.wide on every SM), outside the timed regions
+    p_lo = ctx.measure_int_mul(g3h.G3H_MUL_LO) / 1e12
+    p_hi = ctx.measure_int_mul(g3h.G3H_MUL_HI) / 1e12
+    p_wide = ctx.measure_int_mul(g3h.G3H_MUL_WIDE) / 1e12
+    # the cost of a full 32 x 32 -> 64 product in 32-bit IMAD slots, as measured: a
+    # Montgomery multiply then costs 128 such products and 8 low words
+    wide_slots = p_lo / p_wide
+    mm_measured = 128 * wide_slots + 8
+    red_measured = 64 * wide_slots + 8
+    top_measured = kernel_ops_per_h(LOG_N, nnz_a, nnz_b, mm_ops=mm_measured,
+                                    red_ops=red_measured)[top] / per_h[top]
+    h_measured = sum(kernel_ops_per_h(LOG_N, nnz_a, nnz_b, mm_ops=mm_measured,
+                                      red_ops=red_measured).values())
     roofline = {
         "bound": "alu", "kernel": top, "achieved": achieved, "peak": peak_tops,
         "unit": "T IMAD/s", "frac": achieved / peak_tops, "traffic": traffic,
         "peak_source": "derived: %d SMs x %d 32-bit IMAD results/clk/SM x %.0f MHz; a "
-                       "32x32->64 product counts two" % (SM_COUNT, IMAD_PER_CLK_PER_SM, sm_max),
-        "whole_step_frac": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / peak_tops,
-        "peak_measured": measured_tops,
-        "frac_of_measured": achieved / measured_tops,
-        "whole_step_frac_of_measured": per_h_ops / (step_ms / args.steps * 1e-3) / 1e12 / measured_tops,
+                       "32x32->64 product counts two" % (sms, IMAD_PER_CLK_PER_SM, sm_max),
+        "whole_step_frac": per_h_ops / step_s_1 / 1e12 / peak_tops,
+        "peak_measured": p_lo,
+        "peak_measured_hi": p_hi,
+        "peak_measured_wide": p_wide,
+        "frac_of_measured": achieved / p_lo,
+        "whole_step_frac_of_measured": per_h_ops / step_s_1 / 1e12 / p_lo,
+        "wide_product_slots_measured": wide_slots,
+        "ops_per_mm_measured_slots": mm_measured,
+        "frac_of_measured_in_measured_slots": top_measured / (per_launch_ms * 1e-3) / 1e12 / p_lo,
+        "whole_step_frac_of_measured_in_measured_slots": h_measured / step_s_1 / 1e12 / p_lo,
+        "ncu_heavy_fma_pipe_pct": heavy_pct,
+        "h_ops": per_h_ops,
+        "launch_census_per_h": census,
+        "launch_census_ok": census == {k: float(v) for k, v in per_h.items()},
         "timing": "step times from a pass without per-kernel events (vectors on three "
                   "streams); kernel times from a second pass of the same K steps with the "
                   "library's per-launch events and the three vectors in one launch per "
@@ -742,7 +808,7 @@ def stress_2_22(torch, dev, g3h, synth):
     ctx.sync()
     ctx.close()
     peak = float(measured_peaks().get("hbm_gbs", 0.0)) or None
-    ops = sum(algorithmic_ops(kn, k, 0, 0) for kn in ("ntt_dif", "ntt_mid", "ntt_dit", "join"))
+    ops = h_ops(k, 0, 0, from_witness=False)
     peak_imad = imad_peak()
     return {"h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / peak_imad,
             "ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9,

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libg3h.so")
 SOURCES = [os.path.join(CSRC, "g3h.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fr.cuh", "ntt.cuh", "kernels.cuh", "fq.cuh", "g1.cuh", "msm.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fr.cuh", "ntt.cuh", "kernels.cuh", "fq.cuh", "g1.cuh", "g2.cuh", "msm.cuh")] + [
     os.path.join(ROOT, "include", "g3h.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -123,15 +123,19 @@ __device__ __forceinline__ fr_t fr_mul(const fr_t& a, const fr_t& b) {
 // ---------------------------------------------------------------------------------------
 // Multiplication by a constant (twiddles, shift, scale): Shoup's method (V. Shoup, NTL;
 // D. Harvey, "Faster arithmetic for number-theoretic transforms", J. Symb. Comp. 2014)
-// with beta = 2^256. For a constant w < r store w and w' = floor(w * beta / r); then for
-// any x < beta, q = floor(x * w' / beta) gives x*w - q*r in [0, 2r), since
-// x*w'/beta lies in (x*w/r - 1, x*w/r]. Here q is computed from the columns i + j >= 6 of
-// x * w' only: the dropped columns sum to less than 2^227 < beta, so q is short by at
-// most 1 and x*w - q*r lies in [0, 3r) (exact mod 2^256, as 3r < 2^256); one conditional
-// subtraction of 2r brings it to [0, 2r). With x in Montgomery form (x = X*R) and w in
-// standard form the product is the Montgomery form of X*w, so data never leaves the
-// Montgomery domain. Cost: 43 + 28 full and 16 low-only 32x32 products, against 128 full
-// and 8 low-only for a Montgomery multiply.
+// with beta = 2^256. For a constant w < r store w and w' = floor(w * beta / r), i.e.
+// w * beta = w' * r + e with 0 <= e < r. For x < beta let P = x * w' = Q * beta + rho
+// (0 <= rho < beta); then x * w = Q * r + (rho * r + x * e) / beta, so y = x*w - Q*r lies
+// in [0, 2r). Here the quotient is computed from the columns i + j >= 6 of the limb
+// product x * w' only; the dropped columns sum to D < 6.01 * 2^224 < 2^227, so the
+// quotient q is Q or, when rho < D (the dropped columns would have carried into bit 256),
+// Q - 1. In that case y = (rho * r + x * e) / beta + r, which is below 2r because
+// rho * r + x * e < D * r + x * r <= beta * r whenever x <= beta - D. Every operand the
+// library multiplies is a value in [0, 2r) (2r < beta - 2^227), so y = x*w - q*r lies in
+// [0, 2r) and is exact mod 2^256: no correction step is needed. With x in Montgomery form
+// (x = X*R) and w in standard form the product is the Montgomery form of X*w, so data
+// never leaves the Montgomery domain. Cost: 43 + 2 * 28 full and 16 low-only 32x32
+// products, against 128 full and 8 low-only for a Montgomery multiply.
 struct __align__(16) fr_const_t {
   fr_t w;   // the constant, standard form, < r
   fr_t wp;  // floor(w * 2^256 / r)
@@ -178,15 +182,15 @@ __device__ __forceinline__ void mul_high256_from6(const uint32_t* a, const uint3
   q[7] = c0;
 }
 
-// x * w mod r in [0, 2r) for x < 2^256 and a constant given as (w, w').
+// x * w mod r in [0, 2r) for x < 2^256 - 2^227 (in the library: x < 2r) and a constant
+// given as (w, w'). The bound on x is what makes the truncated quotient safe (above).
 __device__ __forceinline__ fr_t fr_mul_const(const fr_t& x, const fr_t& w, const fr_t& wp) {
   const uint32_t R[8] = {G3H_R0, G3H_R1, G3H_R2, G3H_R3, G3H_R4, G3H_R5, G3H_R6, G3H_R7};
   uint32_t q[8], lxw[8], lqr[8];
   mul_high256_from6(x.v, wp.v, q);
   mul_low256(x.v, w.v, lxw);
   mul_low256(q, R, lqr);
-  fr_t y, d;
-  uint32_t borrow;
+  fr_t y;
   asm("sub.cc.u32  %0, %8,  %16;\n\t"
       "subc.cc.u32 %1, %9,  %17;\n\t"
       "subc.cc.u32 %2, %10, %18;\n\t"
@@ -200,22 +204,6 @@ __device__ __forceinline__ fr_t fr_mul_const(const fr_t& x, const fr_t& w, const
       : "r"(lxw[0]), "r"(lxw[1]), "r"(lxw[2]), "r"(lxw[3]), "r"(lxw[4]), "r"(lxw[5]),
         "r"(lxw[6]), "r"(lxw[7]), "r"(lqr[0]), "r"(lqr[1]), "r"(lqr[2]), "r"(lqr[3]),
         "r"(lqr[4]), "r"(lqr[5]), "r"(lqr[6]), "r"(lqr[7]));
-  asm("sub.cc.u32  %0, %9,  0xe0000002;\n\t"
-      "subc.cc.u32 %1, %10, 0x87c3eb27;\n\t"
-      "subc.cc.u32 %2, %11, 0xf372e122;\n\t"
-      "subc.cc.u32 %3, %12, 0x5067d090;\n\t"
-      "subc.cc.u32 %4, %13, 0x0302b0ba;\n\t"
-      "subc.cc.u32 %5, %14, 0x70a08b6d;\n\t"
-      "subc.cc.u32 %6, %15, 0xc2634053;\n\t"
-      "subc.cc.u32 %7, %16, 0x60c89ce5;\n\t"
-      "subc.u32    %8, 0, 0;"
-      : "=r"(d.v[0]), "=r"(d.v[1]), "=r"(d.v[2]), "=r"(d.v[3]), "=r"(d.v[4]), "=r"(d.v[5]),
-        "=r"(d.v[6]), "=r"(d.v[7]), "=r"(borrow)
-      : "r"(y.v[0]), "r"(y.v[1]), "r"(y.v[2]), "r"(y.v[3]), "r"(y.v[4]), "r"(y.v[5]),
-        "r"(y.v[6]), "r"(y.v[7]));
-  // borrow is 0xffffffff when y < 2r.
-#pragma unroll
-  for (int i = 0; i < 8; i++) y.v[i] = borrow ? y.v[i] : d.v[i];
   return y;
 }
 

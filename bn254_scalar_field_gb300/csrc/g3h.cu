@@ -12,17 +12,21 @@
 // The three vectors' kernels run on three streams (fork/join events), the whole sequence
 // captured once into a CUDA graph per set of pointers and replayed; G3H_SERIALIZE runs the
 // three vectors as one launch per phase on one stream, G3H_FUSED_JOIN writes h from the last
-// forward kernel instead of k_join. Slice kernels come in two builds (ntt.cuh, SliceCfg):
-// radix-4 pass pairs for 2^9 and 2^10 slices, radix-2 passes otherwise.
+// forward kernel instead of k_join. Slice kernels come in three builds (ntt.cuh, SliceCfg):
+// radix-4 pass pairs for slices of 2^9 elements and more, radix-2 passes below.
 //
 // The multiexps over G1 and G2 (msm.cuh) keep their prepared bases in the context.
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "../../include/g3h.h"
@@ -50,6 +54,40 @@ bool host_canonical(const uint32_t* x) {
   }
   return false;  // equal to r
 }
+
+// Host-side fault injection, for tests of the failure paths (no GPU fault is ever made):
+// with the environment variable G3H_FAULT set to "alloc:N", the N-th device or pinned
+// allocation the library attempts fails as if the device were out of memory (the call
+// returns G3H_E_NOMEM); with "cuda:N", the N-th kernel launch or copy it issues is not
+// issued and reports a CUDA error (G3H_E_CUDA). N counts from 1 and the count restarts
+// whenever the variable's value changes; unset, empty or malformed: nothing is injected.
+enum class Fault { alloc, cuda };
+
+bool inject_fault(Fault kind) {
+  static std::mutex mu;
+  static std::string spec;
+  static unsigned long long seen[2] = {0, 0};
+  const char* env = std::getenv("G3H_FAULT");
+  if (!env || !*env) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (spec != env) {
+    spec = env;
+    seen[0] = seen[1] = 0;
+  }
+  const char* name = kind == Fault::alloc ? "alloc:" : "cuda:";
+  const size_t len = std::strlen(name);
+  if (spec.compare(0, len, name) != 0) return false;
+  char* end = nullptr;
+  const unsigned long long n = std::strtoull(spec.c_str() + len, &end, 10);
+  if (!end || *end || n == 0) return false;
+  return ++seen[kind == Fault::alloc ? 0 : 1] == n;
+}
+
+// An NVTX range for the duration of a scope (shown by profilers that record NVTX).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct TimedLaunch {
   const char* name;
@@ -140,6 +178,17 @@ void free_lane_streams(Lane& l) {
     if (e) cudaEventDestroy(e);
 }
 
+// Frees a lane's buffers, streams and events (any of them may be missing).
+void free_lane(Lane& l) {
+  void* lb[] = {l.abc, l.ab_in, l.counters, l.stage};
+  for (void* b : lb)
+    if (b) cudaFree(b);
+  if (l.done) cudaEventDestroy(l.done);
+  free_lane_streams(l);
+  if (l.own_stream && l.stream) cudaStreamDestroy(l.stream);
+  l = Lane();
+}
+
 // The buffers of one group's multiexp (bytes as raw device memory, typed at use).
 struct MsmState {
   uint32_t n = 0;                    // bases prepared
@@ -172,6 +221,7 @@ struct g3h_ctx {
   // constant tables in the (w, w') form of the constant multiply
   fr_const_t *d_tw_fwd = nullptr, *d_tw_inv = nullptr, *d_shift_br = nullptr;
   fr_const_t *d_coset_fwd = nullptr, *d_coset_inv = nullptr;
+  bool coset_ready = false;  // both coset tables allocated and built
   fr_const_t* d_ninv = nullptr;  // n^-1
   fr_t* d_abc = nullptr;  // 3n scratch: a | b | c while they are transformed
   fr_t* d_ab_in = nullptr;  // 2n: the gather's a | b, read by the first inverse kernel
@@ -203,10 +253,18 @@ struct g3h_ctx {
 
 namespace {
 
+int raw_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  if (inject_fault(Fault::alloc)) return G3H_E_NOMEM;
+  return cudaMalloc(p, std::max<size_t>(bytes, 1)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+}
+
 template <class T>
 int dalloc(T** p, size_t count) {
-  if (count == 0) count = 1;
-  return cudaMalloc((void**)p, count * sizeof(T)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+  void* q = nullptr;
+  const int rc = raw_alloc(&q, std::max<size_t>(count, 1) * sizeof(T));
+  *p = (T*)q;
+  return rc;
 }
 
 void msm_free(MsmState& m) {
@@ -227,14 +285,7 @@ void release(g3h_ctx* c) {
   for (void* b : bufs)
     if (b) cudaFree(b);
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
-  for (Lane& l : c->extra_lanes) {
-    void* lb[] = {l.abc, l.ab_in, l.counters, l.stage};
-    for (void* b : lb)
-      if (b) cudaFree(b);
-    if (l.done) cudaEventDestroy(l.done);
-    free_lane_streams(l);
-    if (l.own_stream && l.stream) cudaStreamDestroy(l.stream);
-  }
+  for (Lane& l : c->extra_lanes) free_lane(l);
   free_lane_streams(c->own);
   if (c->batch_start) cudaEventDestroy(c->batch_start);
   for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
@@ -253,6 +304,7 @@ cudaEvent_t take_event(g3h_ctx* c) {
 
 template <class F>
 int run_on(g3h_ctx* c, cudaStream_t st, const char* name, F&& launch) {
+  if (inject_fault(Fault::cuda)) return G3H_E_CUDA;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (c->timing) {
     e0 = take_event(c);
@@ -287,7 +339,7 @@ void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
       case Slice::dif: return k_ntt_dif<2>;
       case Slice::mid: return k_ntt_mid<2>;
       case Slice::dit: return k_ntt_dit<2>;
-      default: break;
+      default: return k_ntt_brev<2>;
     }
   }
   const bool r4 = kk >= kRadix4MinSliceBits && kk <= kRadix4MaxSliceBits && kk >= 2;
@@ -297,7 +349,7 @@ void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
     case Slice::dif: return r4 ? k_ntt_dif<1> : k_ntt_dif<0>;
     case Slice::mid: return r4 ? k_ntt_mid<1> : k_ntt_mid<0>;
     case Slice::dit: return r4 ? k_ntt_dit<1> : k_ntt_dit<0>;
-    default: *threads = std::min(1u << (kk - 1u), kSliceThreads); return k_ntt_brev;
+    default: return r4 ? k_ntt_brev<1> : k_ntt_brev<0>;
   }
 }
 
@@ -316,9 +368,9 @@ int launch_slice(g3h_ctx* c, const char* name, Slice which, const SliceArgs& a, 
 
 int set_smem_limits() {
   const int bytes = 32 << 11;  // the largest slice, 2^11 elements
-  void (*kerns[])(SliceArgs) = {k_ntt_dif<0>, k_ntt_mid<0>, k_ntt_dit<0>, k_ntt_dif<1>,
-                                k_ntt_mid<1>, k_ntt_dit<1>, k_ntt_dif<2>, k_ntt_mid<2>,
-                                k_ntt_dit<2>, k_ntt_brev};
+  void (*kerns[])(SliceArgs) = {k_ntt_dif<0>,  k_ntt_mid<0>, k_ntt_dit<0>, k_ntt_brev<0>,
+                                k_ntt_dif<1>,  k_ntt_mid<1>, k_ntt_dit<1>, k_ntt_brev<1>,
+                                k_ntt_dif<2>,  k_ntt_mid<2>, k_ntt_dit<2>, k_ntt_brev<2>};
   for (auto k : kerns)
     if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
@@ -340,14 +392,25 @@ int build_table(g3h_ctx* c, fr_const_t* tab, size_t count, int base, int scale, 
   });
 }
 
+// The coset tables g^j and g^-j / n, allocated and built by the first coset transform.
+// They count as present only once both are allocated and their builds are enqueued; a
+// failure frees what was allocated, so the next call starts over.
 int ensure_coset_tables(g3h_ctx* c) {
-  if (c->d_coset_fwd) return G3H_OK;
-  int rc = dalloc(&c->d_coset_fwd, c->n);
-  if (rc == G3H_OK) rc = dalloc(&c->d_coset_inv, c->n);
-  if (rc != G3H_OK) return rc;
-  rc = build_table(c, c->d_coset_fwd, c->n, 2, -1, 0);
+  if (c->coset_ready) return G3H_OK;
+  int rc = G3H_OK;
+  if (!c->d_coset_fwd) rc = dalloc(&c->d_coset_fwd, c->n);
+  if (rc == G3H_OK && !c->d_coset_inv) rc = dalloc(&c->d_coset_inv, c->n);
+  if (rc == G3H_OK) rc = build_table(c, c->d_coset_fwd, c->n, 2, -1, 0);
   if (rc == G3H_OK) rc = build_table(c, c->d_coset_inv, c->n, 3, 4, 0);
-  return rc;
+  if (rc != G3H_OK) {
+    cudaStreamSynchronize(c->stream);
+    if (c->d_coset_fwd) cudaFree(c->d_coset_fwd);
+    if (c->d_coset_inv) cudaFree(c->d_coset_inv);
+    c->d_coset_fwd = c->d_coset_inv = nullptr;
+    return rc;
+  }
+  c->coset_ready = true;
+  return G3H_OK;
 }
 
 int ensure_stage(g3h_ctx* c, size_t elems) {
@@ -362,6 +425,7 @@ int ensure_stage(g3h_ctx* c, size_t elems) {
 
 int copy_on(cudaStream_t st, void* dst, const void* src, size_t bytes, cudaMemcpyKind kind) {
   if (bytes == 0) return G3H_OK;
+  if (inject_fault(Fault::cuda)) return G3H_E_CUDA;
   return cudaMemcpyAsync(dst, src, bytes, kind, st) == cudaSuccess ? G3H_OK : G3H_E_CUDA;
 }
 
@@ -415,6 +479,112 @@ Lane lane0(g3h_ctx* c) {
 // buffers. a, b, c may be the lane's scratch vectors. With a witness w (device) instead,
 // steps 1-5: the gather writes a and b and the first inverse kernel forms c = a * b at
 // its load (a, b, c are then ignored).
+//
+// The three vectors are independent until the join: vector v runs on vs[v], so one
+// vector's gather latency and kernel tails overlap the others' transforms. With
+// G3H_SERIALIZE everything runs on the lane's stream, one launch per phase covering the
+// three vectors (grid rows 0, 1, 2), so each kernel runs alone. quotient_vectors issues
+// the work of the forked streams; quotient_launches forks them and always joins them
+// back, also when a launch fails, so that no work is left unjoined (and a stream capture
+// in progress ends cleanly).
+fr_t* s_of(const Lane& ln, size_t n, int v) { return ln.abc + (size_t)v * n; }
+
+int quotient_vectors(g3h_ctx* c, const Lane& ln, const cudaStream_t* vs, bool serial,
+                     const fr_t* a, const fr_t* b, const fr_t* cc, const fr_t* w, fr_t* hm,
+                     fr_t* hs, uint32_t flags) {
+  const uint32_t k = c->log_n;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  const size_t n = c->n;
+  const uint32_t nv = serial ? 1u : 3u;    // launches per phase
+  const unsigned rows = serial ? 3u : 1u;  // vectors per launch
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  int rc = G3H_OK;
+  if (w) {
+    // a and b by the gather, A on the stream of a, B on the stream of b; c = a * b is
+    // formed by c's first inverse kernel at its load, once both are done
+    NvtxRange range("g3h gather");
+    fr_t* ab = ln.ab_in;
+    const uint32_t nn = (uint32_t)n;
+    rc = run_on(c, vs[0], "gather_a", [&] {
+      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(c->d_rpa, c->d_cola, c->d_vala, w,
+                                                            c->n_rows_a, nn, ab, check, c->d_err);
+    });
+    if (rc == G3H_OK)
+      rc = run_on(c, vs[1], "gather_b", [&] {
+        k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
+            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, ab + n, check, c->d_err);
+      });
+    if (rc != G3H_OK) return rc;
+    if (!ok(cudaEventRecord(ln.ev_ga, vs[0])) || !ok(cudaEventRecord(ln.ev_gb, vs[1])) ||
+        !ok(cudaStreamWaitEvent(vs[2], ln.ev_ga, 0)) || !ok(cudaStreamWaitEvent(vs[2], ln.ev_gb, 0)))
+      return G3H_E_CUDA;
+    a = ab;
+    b = ab + n;
+    cc = nullptr;
+  }
+  fr_t* s[3] = {ln.abc, ln.abc + n, ln.abc + 2 * n};
+  const Plan pl = plan_for(k);
+  // Launches are issued phase by phase over the three vectors so that the vectors
+  // advance together.
+  {
+    NvtxRange range("g3h inverse, top levels");
+    for (int lvl = pl.levels - 1; lvl >= 1 && rc == G3H_OK; lvl--) {
+      const bool first = lvl == pl.levels - 1;
+      for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
+        SliceArgs x = base_args(c, flags);
+        x.src[0] = first ? a : s[0];
+        x.src[1] = first ? b : s[1];
+        x.src[2] = first ? cc : s[2];
+        for (int u = 0; u < 3; u++) x.dst[u] = s[u];
+        x.tw = c->d_tw_inv;
+        x.kk = pl.kk[lvl];
+        x.c0 = pl.c0[lvl];
+        x.mode = (first && check && !w) ? SL_CHECK : 0u;
+        if (first && w) x.mode |= SL_C_FROM_AB;
+        x.vbase = v;
+        rc = launch_slice_on(c, vs[v], "ntt_dif", Slice::dif, x, rows);
+      }
+    }
+  }
+  {
+    NvtxRange range("g3h inverse low levels, shift, forward low levels");
+    for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
+      SliceArgs x = base_args(c, flags);
+      for (int u = 0; u < 3; u++) x.dst[u] = s[u];
+      x.tw = c->d_tw_inv;
+      x.tw2 = c->d_tw_fwd;
+      x.scale_tab = c->d_shift_br;
+      x.kk = pl.kk[0];
+      x.c0 = 0;
+      x.vbase = v;
+      rc = launch_slice_on(c, vs[v], "ntt_mid", Slice::mid, x, rows);
+    }
+  }
+  {
+    NvtxRange range("g3h forward, top levels");
+    for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
+      const bool top = lvl == pl.levels - 1;
+      for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
+        SliceArgs x = base_args(c, flags);
+        for (int u = 0; u < 3; u++) x.src[u] = x.dst[u] = s[u];
+        x.tw = c->d_tw_fwd;
+        x.kk = pl.kk[lvl];
+        x.c0 = pl.c0[lvl];
+        x.vbase = v;
+        const bool fused = top && (flags & G3H_FUSED_JOIN);
+        if (fused) {
+          x.mode = SL_JOIN_LAST;
+          x.h_mont = hm;
+          x.h_std = hs;
+          x.counters = ln.counters;
+        }
+        rc = launch_slice_on(c, vs[v], fused ? "ntt_dit_join" : "ntt_dit", Slice::dit, x, rows);
+      }
+    }
+  }
+  return rc;
+}
+
 int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
                       const fr_t* cc, const fr_t* w, fr_t* hm, fr_t* hs, uint32_t flags) {
   const uint32_t k = c->log_n;
@@ -435,103 +605,25 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
                                           hs, k, check, c->d_err);
     });
   }
-  // The three vectors are independent until the join: vector v runs on vs[v], so one
-  // vector's gather latency and kernel tails overlap the others' transforms. With
-  // G3H_SERIALIZE everything runs on the lane's stream, one launch per phase covering
-  // the three vectors (grid rows 0, 1, 2), so each kernel runs alone.
   const bool serial = (flags & G3H_SERIALIZE) != 0u;
   const cudaStream_t vs[3] = {st, serial ? st : ln.aux[0], serial ? st : ln.aux[1]};
-  const uint32_t nv = serial ? 1u : 3u;    // launches per phase
-  const unsigned rows = serial ? 3u : 1u;  // vectors per launch
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-  if (!ok(cudaEventRecord(ln.ev_fork, st)) || !ok(cudaStreamWaitEvent(vs[1], ln.ev_fork, 0)) ||
-      !ok(cudaStreamWaitEvent(vs[2], ln.ev_fork, 0)))
+  if (!serial && (!ok(cudaEventRecord(ln.ev_fork, st)) ||
+                  !ok(cudaStreamWaitEvent(vs[1], ln.ev_fork, 0)) ||
+                  !ok(cudaStreamWaitEvent(vs[2], ln.ev_fork, 0))))
     return G3H_E_CUDA;
-  int rc = G3H_OK;
-  if (w) {
-    // a and b by the gather, A on the stream of a, B on the stream of b; c = a * b is
-    // formed by c's first inverse kernel at its load, once both are done
-    fr_t* ab = ln.ab_in;
-    const uint32_t nn = (uint32_t)n;
-    rc = run_on(c, vs[0], "gather", [&] {
-      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(c->d_rpa, c->d_cola, c->d_vala, w,
-                                                            c->n_rows_a, nn, ab, check, c->d_err);
-    });
-    if (rc == G3H_OK)
-      rc = run_on(c, vs[1], "gather", [&] {
-        k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
-            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, ab + n, check, c->d_err);
-      });
-    if (rc != G3H_OK) return rc;
-    if (!ok(cudaEventRecord(ln.ev_ga, vs[0])) || !ok(cudaEventRecord(ln.ev_gb, vs[1])) ||
-        !ok(cudaStreamWaitEvent(vs[2], ln.ev_ga, 0)) || !ok(cudaStreamWaitEvent(vs[2], ln.ev_gb, 0)))
-      return G3H_E_CUDA;
-    a = ab;
-    b = ab + n;
-    cc = nullptr;
-  }
-  fr_t* s[3] = {ln.abc, ln.abc + n, ln.abc + 2 * n};
-  const Plan pl = plan_for(k);
-  // Launches are issued phase by phase over the three vectors so that the vectors
-  // advance together.
-  // inverse, top levels first
-  for (int lvl = pl.levels - 1; lvl >= 1 && rc == G3H_OK; lvl--) {
-    const bool first = lvl == pl.levels - 1;
-    for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
-      SliceArgs x = base_args(c, flags);
-      x.src[0] = first ? a : s[0];
-      x.src[1] = first ? b : s[1];
-      x.src[2] = first ? cc : s[2];
-      for (int u = 0; u < 3; u++) x.dst[u] = s[u];
-      x.tw = c->d_tw_inv;
-      x.kk = pl.kk[lvl];
-      x.c0 = pl.c0[lvl];
-      x.mode = (first && check && !w) ? SL_CHECK : 0u;
-      if (first && w) x.mode |= SL_C_FROM_AB;
-      x.vbase = v;
-      rc = launch_slice_on(c, vs[v], "ntt_dif", Slice::dif, x, rows);
-    }
-  }
-  for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
-    SliceArgs x = base_args(c, flags);
-    for (int u = 0; u < 3; u++) x.dst[u] = s[u];
-    x.tw = c->d_tw_inv;
-    x.tw2 = c->d_tw_fwd;
-    x.scale_tab = c->d_shift_br;
-    x.kk = pl.kk[0];
-    x.c0 = 0;
-    x.vbase = v;
-    rc = launch_slice_on(c, vs[v], "ntt_mid", Slice::mid, x, rows);
-  }
-  // forward, middle levels, then the top level
-  for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
-    const bool top = lvl == pl.levels - 1;
-    for (uint32_t v = 0; v < nv && rc == G3H_OK; v++) {
-      SliceArgs x = base_args(c, flags);
-      for (int u = 0; u < 3; u++) x.src[u] = x.dst[u] = s[u];
-      x.tw = c->d_tw_fwd;
-      x.kk = pl.kk[lvl];
-      x.c0 = pl.c0[lvl];
-      x.vbase = v;
-      const bool fused = top && (flags & G3H_FUSED_JOIN);
-      if (fused) {
-        x.mode = SL_JOIN_LAST;
-        x.h_mont = hm;
-        x.h_std = hs;
-        x.counters = ln.counters;
-      }
-      rc = launch_slice_on(c, vs[v], fused ? "ntt_dit_join" : "ntt_dit", Slice::dit, x, rows);
-    }
-  }
-  if (rc != G3H_OK) return rc;
+  int rc = quotient_vectors(c, ln, vs, serial, a, b, cc, w, hm, hs, flags);
   // join: the lane's stream waits for vectors b and c
-  for (int i = 0; i < 2; i++)
-    if (!ok(cudaEventRecord(ln.ev_end[i], vs[i + 1])) ||
-        !ok(cudaStreamWaitEvent(st, ln.ev_end[i], 0)))
-      return G3H_E_CUDA;
-  if (flags & G3H_FUSED_JOIN) return G3H_OK;
+  if (!serial)
+    for (int i = 0; i < 2; i++)
+      if (!ok(cudaEventRecord(ln.ev_end[i], vs[i + 1])) ||
+          !ok(cudaStreamWaitEvent(st, ln.ev_end[i], 0)))
+        rc = G3H_E_CUDA;
+  if (rc != G3H_OK || (flags & G3H_FUSED_JOIN)) return rc;
+  NvtxRange range("g3h join");
   return run_on(c, st, "join", [&] {
-    k_join<<<blocks_for(n, 256), 256, 0, st>>>(s[0], s[1], s[2], hm, hs, n, 0u, c->d_err);
+    k_join<<<blocks_for(n, 256), 256, 0, st>>>(s_of(ln, n, 0), s_of(ln, n, 1), s_of(ln, n, 2), hm,
+                                                hs, n, 0u, c->d_err);
   });
 }
 
@@ -738,7 +830,10 @@ int g3h_prepare(uint32_t log_n, uint32_t n_wires, const g3h_csr* A, const g3h_cs
   rc = set_smem_limits();
   if (rc == G3H_OK) rc = make_lane_streams(c->own);
   if (rc == G3H_OK)
-    rc = cudaMallocHost((void**)&c->h_err, sizeof(uint32_t)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
+    rc = !inject_fault(Fault::alloc) &&
+                 cudaMallocHost((void**)&c->h_err, sizeof(uint32_t)) == cudaSuccess
+             ? G3H_OK
+             : G3H_E_NOMEM;
   if (rc == G3H_OK) *c->h_err = 0;
   if (rc == G3H_OK) rc = dalloc(&c->d_err, 1);
   if (rc == G3H_OK)
@@ -791,6 +886,7 @@ int g3h_compute_h(g3h_ctx* c, const uint32_t* witness, uint32_t* h_mont, uint32_
                   uint32_t flags) {
   if (!c || !c->has_csr || !h_mont || !h_std || (!witness && c->n_wires)) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
+  NvtxRange range("g3h_compute_h");
   const size_t n = c->n;
   fr_t* s[3] = {c->d_abc, c->d_abc + n, c->d_abc + 2 * n};
   if ((flags & G3H_DEVICE_PTRS) && misaligned({witness, h_mont, h_std})) return G3H_E_INVAL;
@@ -814,6 +910,7 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
                       uint32_t* h_mont, uint32_t* h_std, uint32_t flags) {
   if (!c || !a || !b || !cc || !h_mont || !h_std) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
+  NvtxRange range("g3h_compute_h_abc");
   const size_t n = c->n;
   if ((flags & G3H_DEVICE_PTRS) && misaligned({a, b, cc, h_mont, h_std})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
@@ -847,20 +944,26 @@ int ensure_lanes(g3h_ctx* c, uint32_t lanes, bool staged) {
   const Plan pl = plan_for(c->log_n);
   const size_t n_slices = std::max<size_t>(n >> pl.kk[pl.levels - 1], 1);
   while (c->extra_lanes.size() + 1 < lanes) {
-    c->extra_lanes.emplace_back();
-    Lane& l = c->extra_lanes.back();
-    if (cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) != cudaSuccess)
-      return G3H_E_CUDA;
-    l.own_stream = true;
-    int rc = dalloc(&l.abc, 3 * n);
+    // a lane joins the context only once all its parts exist
+    Lane l;
+    int rc = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) == cudaSuccess
+                 ? G3H_OK
+                 : G3H_E_CUDA;
+    l.own_stream = l.stream != nullptr;
+    if (rc == G3H_OK) rc = dalloc(&l.abc, 3 * n);
     if (rc == G3H_OK) rc = dalloc(&l.ab_in, 2 * n);
     if (rc == G3H_OK) rc = dalloc(&l.counters, n_slices);
-    if (rc != G3H_OK) return rc;
-    if (cudaMemsetAsync(l.counters, 0, n_slices * sizeof(uint32_t), l.stream) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess)
-      return G3H_E_CUDA;
-    rc = make_lane_streams(l);
-    if (rc != G3H_OK) return rc;
+    if (rc == G3H_OK &&
+        (cudaMemsetAsync(l.counters, 0, n_slices * sizeof(uint32_t), l.stream) != cudaSuccess ||
+         cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess))
+      rc = G3H_E_CUDA;
+    if (rc == G3H_OK) rc = make_lane_streams(l);
+    if (rc != G3H_OK) {
+      if (l.stream) cudaStreamSynchronize(l.stream);
+      free_lane(l);
+      return rc;
+    }
+    c->extra_lanes.push_back(l);
   }
   if (!c->batch_start &&
       cudaEventCreateWithFlags(&c->batch_start, cudaEventDisableTiming) != cudaSuccess)
@@ -893,6 +996,7 @@ int g3h_compute_h_batch(g3h_ctx* c, uint32_t count, const uint32_t* witnesses,
   if (count == 0) return G3H_OK;
   if (!h_mont || !h_std || (!witnesses && c->n_wires)) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
+  NvtxRange range("g3h_compute_h_batch");
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0u;
   if (dev && misaligned({witnesses, h_mont, h_std})) return G3H_E_INVAL;
   const uint32_t lanes = std::min(count, kBatchLanes);
@@ -941,6 +1045,7 @@ int g3h_gather(g3h_ctx* c, const uint32_t* witness, uint32_t* a, uint32_t* b, ui
                uint32_t flags) {
   if (!c || !c->has_csr || !a || !b || !cc || (!witness && c->n_wires)) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
+  NvtxRange range("g3h_gather");
   const size_t n = c->n;
   if ((flags & G3H_DEVICE_PTRS) && misaligned({witness, a, b, cc})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS)
@@ -961,6 +1066,7 @@ int g3h_gather(g3h_ctx* c, const uint32_t* witness, uint32_t* a, uint32_t* b, ui
 int g3h_ntt(g3h_ctx* c, uint32_t* data, int inverse, int coset, uint32_t flags) {
   if (!c || !data) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
+  NvtxRange range("g3h_ntt");
   const size_t n = c->n;
   if ((flags & G3H_DEVICE_PTRS) && misaligned({data})) return G3H_E_INVAL;
   if (flags & G3H_DEVICE_PTRS) return ntt(c, (fr_t*)data, inverse, coset, flags);
@@ -1174,9 +1280,7 @@ int msm_prepare(g3h_ctx* c, MsmState& m, const uint32_t* bases, uint32_t n_bases
   msm_free(m);
   if (n_bases == 0) return G3H_OK;
   const size_t n = n_bases;
-  auto alloc = [](void** p, size_t bytes) {
-    return cudaMalloc(p, std::max<size_t>(bytes, 1)) == cudaSuccess ? G3H_OK : G3H_E_NOMEM;
-  };
+  auto alloc = [](void** p, size_t bytes) { return raw_alloc(p, bytes); };
   int rc = alloc(&m.table, n * kMsmWindows * sizeof(Aff));
   if (rc == G3H_OK) rc = dalloc(&m.entries, n * kMsmWindows);
   // per-bucket counters, then the long-run list: its count and up to kMsmBuckets indices
@@ -1227,6 +1331,7 @@ int msm_run(g3h_ctx* c, MsmState& m, const uint32_t* scalars, uint32_t count, ui
   if (!c || !result || (!scalars && count)) return G3H_E_INVAL;
   if (count > m.n) return G3H_E_RANGE;
   DeviceGuard guard(c->device);
+  NvtxRange range(G::kName);
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0;
   if (dev && misaligned({scalars, result})) return G3H_E_INVAL;
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
@@ -1345,58 +1450,75 @@ int g3h_timing_read(g3h_ctx* c, g3h_kernel_time* out, int max, int* count) {
 
 namespace g3h {
 
-// Throughput probe of the integer multiply pipe, for the roofline's denominator (32-bit
-// IMAD results per second): eight independent chains of 32-bit multiply-adds
-// (mad.lo.u32, y <- y * c + a) per thread, sixteen per chain and loop iteration; every
-// product takes the chain's value so far, so none can be computed once and reused.
+// Throughput probes of the integer multiply pipe, for the roofline's denominator: eight
+// independent chains per thread, sixteen steps per chain and loop iteration, of
+//   KIND 0: 32-bit multiply-adds, low word (mad.lo.u32, y <- y * c + a);
+//   KIND 1: 32-bit multiply-adds, high word (mad.hi.u32, y <- hi(y * c) + a);
+//   KIND 2: full 32 x 32 -> 64-bit multiply-adds (mad.wide.u32, x <- lo(x) * c + x).
+// Every product takes the chain's value so far, so none can be computed once and reused.
 // Nothing is read; sink[0] is written only if the chains' final values XOR to `seed`,
 // which keeps them live. Launch: any grid of 256 threads.
-__global__ void __launch_bounds__(256) k_imad_probe(uint32_t* sink, uint32_t iters, uint32_t seed) {
+template <int KIND>
+__global__ void __launch_bounds__(256) k_imad_probe(uint64_t* sink, uint32_t iters, uint32_t seed) {
   uint32_t y[8], a[8];
+  uint64_t x[8];
 #pragma unroll
   for (int k = 0; k < 8; k++) {
     a[k] = seed * (threadIdx.x + 1u) + (uint32_t)k * 0x9e3779b9u;
     y[k] = a[k];
+    x[k] = a[k];
   }
   const uint32_t c = seed ^ (blockIdx.x * 0x85ebca6bu);
   for (uint32_t it = 0; it < iters; it++) {
 #pragma unroll
     for (int r = 0; r < 16; r++) {
 #pragma unroll
-      for (int k = 0; k < 8; k++)
-        asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(y[k]) : "r"(c ^ a[k]), "r"(a[k]));
+      for (int k = 0; k < 8; k++) {
+        if (KIND == 0)
+          asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(y[k]) : "r"(c ^ a[k]), "r"(a[k]));
+        else if (KIND == 1)
+          asm volatile("mad.hi.u32 %0, %0, %1, %2;" : "+r"(y[k]) : "r"(c ^ a[k]), "r"(a[k]));
+        else
+          asm volatile("{\n\t.reg .u32 lo;\n\tcvt.u32.u64 lo, %0;\n\tmad.wide.u32 %0, lo, %1, %0;\n\t}"
+                       : "+l"(x[k]) : "r"(c ^ a[k]));
+      }
     }
   }
-  uint32_t s = 0;
+  uint64_t s = 0;
 #pragma unroll
-  for (int k = 0; k < 8; k++) s ^= y[k];
-  if (s == seed) sink[0] = s;
+  for (int k = 0; k < 8; k++) s ^= (uint64_t)y[k] ^ x[k];
+  if (s == (uint64_t)seed) sink[0] = s;
 }
 
 }  // namespace g3h
 
-extern "C" {
+namespace {
 
-int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
-  if (!c || !results_per_s) return G3H_E_INVAL;
+int measure_mul(g3h_ctx* c, int kind, double* per_s) {
+  if (!c || !per_s || kind < 0 || kind > 2) return G3H_E_INVAL;
   DeviceGuard guard(c->device);
-  uint32_t* sink = nullptr;
-  if (cudaMalloc((void**)&sink, sizeof(uint32_t)) != cudaSuccess) return G3H_E_NOMEM;
+  uint64_t* sink = nullptr;
+  if (cudaMalloc((void**)&sink, sizeof(uint64_t)) != cudaSuccess) return G3H_E_NOMEM;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   int rc = cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess
                ? G3H_OK
                : G3H_E_CUDA;
-  // four blocks of eight warps per SM; about 4 ms a run at 2 x 10^13 results per second
+  // four blocks of eight warps per SM; a few ms a run
   const unsigned grid = (unsigned)c->sm_count * 4;
-  const uint32_t iters = 4096;
+  const uint32_t iters = kind == 0 ? 4096u : 2048u;
+  auto launch = [&](uint32_t it, uint32_t seed) {
+    if (kind == 0) k_imad_probe<0><<<grid, 256, 0, c->stream>>>(sink, it, seed);
+    else if (kind == 1) k_imad_probe<1><<<grid, 256, 0, c->stream>>>(sink, it, seed);
+    else k_imad_probe<2><<<grid, 256, 0, c->stream>>>(sink, it, seed);
+  };
   double best = 0.0;
   for (int run = 0; run < 4 && rc == G3H_OK; run++) {
     const uint32_t it = run == 0 ? 64u : iters;  // the first run warms up
-    k_imad_probe<<<grid, 256, 0, c->stream>>>(sink, it, 0x2545f491u + (uint32_t)run);
+    launch(it, 0x2545f491u + (uint32_t)run);
     if (cudaGetLastError() != cudaSuccess) rc = G3H_E_CUDA;
     if (run == 0 || rc != G3H_OK) continue;
     cudaEventRecord(e0, c->stream);
-    k_imad_probe<<<grid, 256, 0, c->stream>>>(sink, it, 0x9e3779b1u + (uint32_t)run);
+    launch(it, 0x9e3779b1u + (uint32_t)run);
     cudaEventRecord(e1, c->stream);
     float ms = 0.f;
     if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
@@ -1404,15 +1526,27 @@ int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
       rc = G3H_E_CUDA;
       continue;
     }
-    const double results = (double)grid * 256.0 * it * 16.0 * 8.0;
-    best = std::max(best, results / (ms * 1e-3));
+    const double ops = (double)grid * 256.0 * it * 16.0 * 8.0;
+    best = std::max(best, ops / (ms * 1e-3));
   }
   if (rc == G3H_OK && cudaStreamSynchronize(c->stream) != cudaSuccess) rc = G3H_E_CUDA;
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
   cudaFree(sink);
-  if (rc == G3H_OK) *results_per_s = best;
+  if (rc == G3H_OK) *per_s = best;
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
+  return measure_mul(c, G3H_MUL_LO, results_per_s);
+}
+
+int g3h_measure_int_mul(g3h_ctx* c, int kind, double* per_s) {
+  return measure_mul(c, kind, per_s);
 }
 
 }  // extern "C"
@@ -1421,9 +1555,8 @@ int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
 // g3h_compute_h_abc_static: steps 2-5 without any allocation.
 //
 // For callers that cannot allocate device memory themselves or through this library: a
-// framework whose caching allocator must own every device byte, code that runs while its
-// stream is being captured into a CUDA graph (where cudaMalloc is not permitted), or
-// latency-critical paths that cannot afford cudaMalloc's device-wide synchronisation.
+// framework whose caching allocator must own every device byte, or a latency-critical path
+// that cannot take cudaMalloc's device-wide synchronisation.
 // The working vectors and the domain tables live in one file-scope device array of fixed
 // size, reserved on every GPU that loads this library until the process exits:
 // (in 32-byte elements; a table entry (w, w') takes two)
@@ -1432,9 +1565,14 @@ int g3h_measure_imad(g3h_ctx* c, double* results_per_s) {
 //   [4N, 5N)         inverse twiddles omega^-j, j < n/2
 //   [5N, 7N)         shift table g^brev(p) / n
 //   [7N, 7N + 6)     domain constants
+//   [7N + 6]         word 0: log_n + 1 of the domain whose tables [3N, 7N + 6) hold, 0 for
+//                    none (the array starts zeroed when the library is loaded)
 // with N = 2^16, the largest domain this entry point accepts: 7N + 8 elements of 32 bytes,
-// 14 MiB. Every element of the array that a call reads was written earlier in the same
-// call or by the table build for the same domain, so nothing has to start at zero.
+// 14 MiB. Whether the tables match a call's log_n is decided on the GPU, in stream order,
+// by that call's own table kernels (k_static_domain, k_static_tables, k_static_tag): the
+// host keeps no record of it, so the outcome does not depend on which calls the host made
+// before. Every other element of the array that a call reads was written earlier in the
+// same call, so nothing else has to start at zero.
 namespace {
 constexpr uint32_t kNoAllocMaxLog = 16;
 constexpr size_t kNoAllocN = (size_t)1 << kNoAllocMaxLog;
@@ -1443,14 +1581,40 @@ constexpr size_t kNoAllocElems = 7 * kNoAllocN + 8;
 
 static __device__ __align__(256) fr_t g3h_noalloc_scratch[kNoAllocElems];
 
+namespace g3h {
+
+// The domain constants of 2^k into consts, unless *tag says the tables already hold 2^k.
+// Launch: 1 block of 1 thread.
+__global__ void k_static_domain(fr_t* consts, const uint32_t* tag, uint32_t k) {
+  if (*tag == k + 1u) return;
+  domain_constants(consts, k);
+}
+
+// The three tables of 2^k (forward and inverse twiddles, n/2 entries each, and the shift
+// table, n entries), one entry per thread, unless *tag says they already hold 2^k.
+// Launch: ceil(2n / 256) x 256.
+__global__ void k_static_tables(fr_const_t* tw_fwd, fr_const_t* tw_inv, fr_const_t* shift,
+                                const fr_t* consts, const uint32_t* tag, uint32_t k) {
+  if (*tag == k + 1u) return;
+  const size_t n = (size_t)1 << k, half = n >> 1;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < half)
+    tw_fwd[i] = pow_table_entry(consts, 0, -1, (uint32_t)i);
+  else if (i < 2 * half)
+    tw_inv[i - half] = pow_table_entry(consts, 1, -1, (uint32_t)(i - half));
+  else if (i < 2 * half + n)
+    shift[i - 2 * half] = pow_table_entry(consts, 2, 4, bitrev((uint32_t)(i - 2 * half), k));
+}
+
+// Records that the tables hold 2^k. Launch: 1 block of 1 thread, after k_static_tables.
+__global__ void k_static_tag(uint32_t* tag, uint32_t k) { *tag = k + 1u; }
+
+}  // namespace g3h
+
 namespace {
 
-struct NoAllocDevice {
-  fr_t* base = nullptr;  // device address of g3h_noalloc_scratch on this device
-  int table_log = -1;    // domain whose tables the array currently holds
-};
 constexpr int kNoAllocMaxDevices = 64;
-NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+fr_t* g_noalloc_base[kNoAllocMaxDevices];  // device address of the array, per device
 std::mutex g_noalloc_mu;
 
 int noalloc_launch_ok() { return cudaGetLastError() == cudaSuccess ? G3H_OK : G3H_E_CUDA; }
@@ -1466,33 +1630,31 @@ extern "C" int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
     return G3H_E_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  NoAllocDevice& d = g_noalloc[dev];
-  if (!d.base) {
-    // One-time set-up on this device (the device is current): the host-side name of the
-    // array is not a device address, so ask the runtime for the address.
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g3h_noalloc_scratch) != cudaSuccess || !p) return G3H_E_CUDA;
-    d.base = (fr_t*)p;
+  fr_t* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+      // One-time set-up on this device (the device is current): the host-side name of the
+      // array is not a device address, so ask the runtime for the address.
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g3h_noalloc_scratch) != cudaSuccess || !p) return G3H_E_CUDA;
+      g_noalloc_base[dev] = (fr_t*)p;
+    }
+    base = g_noalloc_base[dev];
   }
   const cudaStream_t s = (cudaStream_t)stream;
   const size_t n = (size_t)1 << log_n;
-  fr_t* work = d.base;
-  fr_const_t* tw_fwd = reinterpret_cast<fr_const_t*>(d.base + 3 * kNoAllocN);
+  fr_t* work = base;
+  fr_const_t* tw_fwd = reinterpret_cast<fr_const_t*>(base + 3 * kNoAllocN);
   fr_const_t* tw_inv = tw_fwd + kNoAllocN / 2;
   fr_const_t* shift = tw_inv + kNoAllocN / 2;
   fr_t* consts = reinterpret_cast<fr_t*>(shift + kNoAllocN);
-  if (d.table_log != (int)log_n) {
-    d.table_log = -1;
-    k_domain<<<1, 1, 0, s>>>(consts, log_n);
-    if (n / 2)
-      k_pow_table<<<blocks_for(n / 2, 256), 256, 0, s>>>(tw_fwd, n / 2, consts, 0, -1, 0);
-    if (n / 2)
-      k_pow_table<<<blocks_for(n / 2, 256), 256, 0, s>>>(tw_inv, n / 2, consts, 1, -1, 0);
-    k_pow_table<<<blocks_for(n, 256), 256, 0, s>>>(shift, n, consts, 2, 4, log_n);
-    if (noalloc_launch_ok() != G3H_OK) return G3H_E_CUDA;
-    d.table_log = (int)log_n;
-  }
+  uint32_t* tag = reinterpret_cast<uint32_t*>(consts + 6);
+  k_static_domain<<<1, 1, 0, s>>>(consts, tag, log_n);
+  k_static_tables<<<blocks_for(2 * n, 256), 256, 0, s>>>(tw_fwd, tw_inv, shift, consts, tag,
+                                                          log_n);
+  k_static_tag<<<1, 1, 0, s>>>(tag, log_n);
+  if (noalloc_launch_ok() != G3H_OK) return G3H_E_CUDA;
   const fr_t* in[3] = {(const fr_t*)a, (const fr_t*)b, (const fr_t*)c};
   fr_t* hm = (fr_t*)h_mont;
   fr_t* hs = (fr_t*)h_std;

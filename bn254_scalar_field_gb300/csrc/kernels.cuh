@@ -299,8 +299,7 @@ __device__ fr_t fr_pow_u32(const fr_t& base, uint32_t e) {
 // Domain constants for 2^k, Montgomery form: out[0] = omega, out[1] = omega^-1, out[2] = g,
 // out[3] = g^-1, out[4] = n^-1, out[5] = 1. The 2^28-th root of unity is 5^((r-1)/2^28)
 // (5 is a quadratic non-residue mod r); g = that root to the 2^(27-k), omega = g^2.
-// Launch: 1 block of 1 thread.
-__global__ void k_domain(fr_t* out, uint32_t k) {
+__device__ void domain_constants(fr_t* out, uint32_t k) {
   fr_t w = fr_pow_limbs(fr_small_mont(5u), kOddPart);
   for (uint32_t i = 0; i < 27u - k; i++) w = fr_canon(fr_mul(w, w));
   const fr_t g = w;
@@ -313,22 +312,31 @@ __global__ void k_domain(fr_t* out, uint32_t k) {
   out[5] = fr_one_mont();
 }
 
-// tab[i] = the constant scale * base^(bit-reversed i if brev_bits else i), i < count, in
-// the (w, w') form of the constant multiply; base and scale are indices into the domain
-// constants (scale < 0: none). The power is formed in Montgomery form x = w*R mod r, then
-// w = from_mont(x) and w' = x * (-r^-1) mod 2^256. Launch: ceil(count/256) x 256.
-__global__ void k_pow_table(fr_const_t* tab, size_t count, const fr_t* consts, int base_idx,
-                            int scale_idx, uint32_t brev_bits) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const uint32_t e = brev_bits ? bitrev((uint32_t)i, brev_bits) : (uint32_t)i;
+// Launch: 1 block of 1 thread.
+__global__ void k_domain(fr_t* out, uint32_t k) { domain_constants(out, k); }
+
+// The constant scale * base^e in the (w, w') form of the constant multiply; base and scale
+// are indices into the domain constants (scale < 0: none). The power is formed in
+// Montgomery form x = w*R mod r, then w = from_mont(x) and w' = x * (-r^-1) mod 2^256.
+__device__ __forceinline__ fr_const_t pow_table_entry(const fr_t* consts, int base_idx,
+                                                      int scale_idx, uint32_t e) {
   fr_t x = fr_pow_u32(consts[base_idx], e);
   if (scale_idx >= 0) x = fr_canon(fr_mul(x, consts[scale_idx]));
   const uint32_t ninv[8] = G3H_NINV256;
   fr_const_t c;
   c.w = fr_from_mont(x);
   mul_low256(x.v, ninv, c.wp.v);
-  tab[i] = c;
+  return c;
+}
+
+// tab[i] = pow_table_entry(base^(bit-reversed i if brev_bits else i)), i < count.
+// Launch: ceil(count/256) x 256.
+__global__ void k_pow_table(fr_const_t* tab, size_t count, const fr_t* consts, int base_idx,
+                            int scale_idx, uint32_t brev_bits) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const uint32_t e = brev_bits ? bitrev((uint32_t)i, brev_bits) : (uint32_t)i;
+  tab[i] = pow_table_entry(consts, base_idx, scale_idx, e);
 }
 
 }  // namespace g3h

@@ -246,6 +246,7 @@ struct G1 {
   using Aff = g1_aff_t;
   using Pt = g1_xyzz_t;
   using F = fq_t;
+  static constexpr const char* kName = "g3h_msm";
   static constexpr uint32_t kTree = 256;
   static __device__ __forceinline__ Pt inf() { return xyzz_infinity(); }
   static __device__ __forceinline__ bool aff_inf(const Aff& a) { return aff_is_inf(a); }
@@ -276,6 +277,7 @@ struct G2 {
   using Aff = g2_aff_t;
   using Pt = g2_xyzz_t;
   using F = fq2_t;
+  static constexpr const char* kName = "g3h_msm_g2";
   static constexpr uint32_t kTree = 128;
   static __device__ __forceinline__ Pt inf() { return g2_infinity(); }
   static __device__ __forceinline__ bool aff_inf(const Aff& a) { return g2_aff_is_inf(a); }

@@ -129,10 +129,6 @@ __device__ __forceinline__ fr_t gather_c(const fr_t& a, const fr_t& b) {
   return (fr_is_zero(a) || fr_is_zero(b)) ? fr_zero() : fr_canon(fr_mul(a, b));
 }
 
-// Threads of the radix-2 k_ntt_brev kernel: one per butterfly up to kSliceThreads, four
-// resident blocks per SM. The other slice kernels' builds: SliceCfg below.
-constexpr uint32_t kSliceThreads = 256;
-
 // Butterfly of the pass on slice bit lb: index bf in [0, 2^(kk-1)) -> lower element lo,
 // upper element lo + 2^lb, and the twiddle table index of the element bit c0 + lb:
 // j = (element index of lo) mod 2^(c0+lb) = low + ((lo mod 2^lb) << c0), times
@@ -476,12 +472,15 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 
 // ---------------------------------------------------------------------------------------
 // k_ntt_brev: the first decimation-in-time passes (bits 0 .. kk-1) of a natural-order
-// forward transform, on the contiguous slice at blockIdx.x << kk: position i loads
-// src[brev(i)] (the bit-reversal permutation absorbed into the load, as on the NTT_CU
-// page), scaled by scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and
-// the result goes to dst (out of place: a block reads other blocks' elements).
-// Launch: grid (n >> kk), block min(2^(kk-1), 256), shared 2^kk * 32 bytes.
-__global__ void __launch_bounds__(kSliceThreads, 4) k_ntt_brev(const __grid_constant__ SliceArgs p) {
+// transform, on the contiguous slice at blockIdx.x << kk: position i loads src[brev(i)]
+// (the bit-reversal permutation absorbed into the load, as on the NTT_CU page), scaled by
+// scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and the result goes to
+// dst (out of place: a block reads other blocks' elements). The passes are those of the
+// slice build C (radix-4 pass pairs in builds 1 and 2). Every 32-byte element is one
+// sector, so the scattered loads read no byte they do not use.
+// Launch: grid (n >> kk), block as the build's other kernels, shared 2^kk * 32 bytes.
+template <int C>
+__global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_brev(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)blockIdx.x << kk;
@@ -494,7 +493,7 @@ __global__ void __launch_bounds__(kSliceThreads, 4) k_ntt_brev(const __grid_cons
     sm_put(sm, size, m, x);
   }
   __syncthreads();
-  for (uint32_t lb = 0; lb < kk; lb++) dit_pass(sm, kk, p.tw, lb, 0u, 0u, k);
+  dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw, 0u, 0u, k);
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(p.dst[0] + base + m, sm_get(sm, size, m));
 }

@@ -30,6 +30,10 @@ G3H_FUSED_JOIN = 0x4
 G3H_SERIALIZE = 0x8
 G3H_NO_GRAPH = 0x10
 
+G3H_MUL_LO = 0
+G3H_MUL_HI = 1
+G3H_MUL_WIDE = 2
+
 G3H_MAX_LOG_N = 27
 G3H_MSM_MAX_LOG = 24
 
@@ -40,7 +44,8 @@ ENTRY_POINTS = ("g3h_prepare", "g3h_compute_h", "g3h_compute_h_abc", "g3h_gather
                 "g3h_join", "g3h_mul", "g3h_sync", "g3h_destroy", "g3h_strerror", "g3h_info",
                 "g3h_timing_enable", "g3h_timing_read", "g3h_compute_h_abc_static",
                 "g3h_compute_h_batch", "g3h_mont_to_std", "g3h_msm_prepare", "g3h_msm",
-                "g3h_msm_g2_prepare", "g3h_msm_g2", "g3h_measure_imad")
+                "g3h_msm_g2_prepare", "g3h_msm_g2", "g3h_measure_imad",
+                "g3h_measure_int_mul")
 
 
 class G3HError(RuntimeError):
@@ -96,6 +101,7 @@ def lib():
         L.g3h_compute_h_abc_static.argtypes = [U, P, P, P, P, P, P]
         L.g3h_compute_h_batch.argtypes = [P, U, P, P, P, U]
         L.g3h_measure_imad.argtypes = [P, ctypes.POINTER(ctypes.c_double)]
+        L.g3h_measure_int_mul.argtypes = [P, I, ctypes.POINTER(ctypes.c_double)]
         for name in ENTRY_POINTS:
             if name not in ("g3h_destroy", "g3h_strerror"):
                 getattr(L, name).restype = ctypes.c_int
@@ -291,6 +297,14 @@ def g3h_measure_imad(ctx):
     return v.value
 
 
+def g3h_measure_int_mul(ctx, kind):
+    """Thread-level instructions per second of independent mad.lo / mad.hi / mad.wide
+    chains (kind G3H_MUL_LO, G3H_MUL_HI, G3H_MUL_WIDE)."""
+    v = ctypes.c_double()
+    _check(lib().g3h_measure_int_mul(ctx, int(kind), ctypes.byref(v)), "g3h_measure_int_mul")
+    return v.value
+
+
 def g3h_sync(ctx):
     _check(lib().g3h_sync(ctx), "g3h_sync")
 
@@ -386,6 +400,9 @@ class Context:
 
     def measure_imad(self):
         return g3h_measure_imad(self.handle)
+
+    def measure_int_mul(self, kind):
+        return g3h_measure_int_mul(self.handle, kind)
 
     def sync(self):
         g3h_sync(self.handle)

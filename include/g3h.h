@@ -55,7 +55,8 @@ extern "C" {
 #endif
 
 #define G3H_OK 0
-#define G3H_E_INVAL (-1)    /* NULL pointer, bad size, call not valid for this context */
+#define G3H_E_INVAL (-1)    /* NULL pointer, device pointer not 16-byte aligned, bad size,
+                               call not valid for this context */
 #define G3H_E_NONCANON (-2) /* an input field element is >= r */
 #define G3H_E_RANGE (-3)    /* log_n outside [0, 27]; CSR row pointers not monotone, not
                                starting at 0, or a column index >= n_wires */
@@ -124,14 +125,14 @@ int g3h_compute_h(g3h_ctx* ctx, const uint32_t* witness, uint32_t* h_mont, uint3
 int g3h_compute_h_abc(g3h_ctx* ctx, const uint32_t* a, const uint32_t* b, const uint32_t* c,
                       uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
 
-/* Steps 1-5 for `count` witnesses over the same prepared matrices (SURVEY's first
- * "next" item, batched H): witness i is the n_wires elements at witnesses + 8*n_wires*i,
- * its outputs the n elements at h_mont + 8*n*i and h_std + 8*n*i. Consecutive witnesses
- * run on up to three streams with their own buffers (allocated by the first batched call
- * and kept by the context), so that one computation's gather and kernel tails overlap
- * another's transforms and, with host pointers, its copies (use pinned host memory for
- * the copies to overlap). The batch completes in the order of the context's stream.
- * Results are those of count separate g3h_compute_h calls. count = 0 does nothing. */
+/* Steps 1-5 for `count` witnesses over the same prepared matrices (batched H): witness i
+ * is the n_wires elements at witnesses + 8*n_wires*i, its outputs the n elements at
+ * h_mont + 8*n*i and h_std + 8*n*i. Consecutive witnesses run on up to three streams with
+ * their own buffers (allocated by the first batched call and kept by the context), so
+ * that one computation's gather and kernel tails overlap another's transforms and, with
+ * host pointers, its copies (use pinned host memory for the copies to overlap). The batch
+ * completes in the order of the context's stream. Results are those of count separate
+ * g3h_compute_h calls. count = 0 does nothing. */
 int g3h_compute_h_batch(g3h_ctx* ctx, uint32_t count, const uint32_t* witnesses,
                         uint32_t* h_mont, uint32_t* h_std, uint32_t flags);
 
@@ -208,10 +209,9 @@ int g3h_msm_g2(g3h_ctx* ctx, const uint32_t* scalars, uint32_t count, uint32_t* 
                uint32_t flags);
 
 /* Steps 2-5 like g3h_compute_h_abc, for callers that cannot allocate device memory: a
- * framework whose caching allocator must own every device byte, code running while its
- * stream is being captured into a CUDA graph (cudaMalloc is not permitted there), or a
- * latency-critical path that cannot take cudaMalloc's device-wide synchronisation. It has
- * no counterpart on the pages; it is this library's own addition.
+ * framework whose caching allocator must own every device byte, or a latency-critical
+ * path that cannot take cudaMalloc's device-wide synchronisation. It has no counterpart
+ * on the pages; it is this library's own addition.
  *
  * It needs no context and allocates nothing: its working vectors and domain tables live in
  * one fixed device array of 14 MiB inside the library, reserved on every GPU that loads
@@ -219,17 +219,21 @@ int g3h_msm_g2(g3h_ctx* ctx, const uint32_t* scalars, uint32_t count, uint32_t* 
  * larger domains return G3H_E_RANGE without doing anything.
  *
  * a, b, c (inputs, n elements each, Montgomery, canonical; NOT checked) and h_mont, h_std
- * (outputs, n elements each) are device pointers on the current CUDA device; `stream` is
- * the cudaStream_t to run on (NULL: the legacy default stream). The call enqueues the work
- * and returns; the outputs are ready when the stream reaches that point.
+ * (outputs, n elements each) are device pointers on the current CUDA device, each 16-byte
+ * aligned; `stream` is the cudaStream_t to run on (NULL: the legacy default stream). The
+ * call enqueues the work and returns; the outputs are ready when the stream reaches that
+ * point.
  *
  * The first call on a device looks up the array's device address (a one-time set-up with
- * that device current); make that first call before any stream capture begins. A call for
- * a different log_n than the previous call on that device also rebuilds the tables in the
- * array (kernel launches only). All calls on a device share the array, so calls that
- * overlap on the GPU (on different streams, or from different threads without ordering)
- * race and give wrong results: order them on one stream.
- * Returns G3H_OK, G3H_E_INVAL (a NULL pointer), G3H_E_RANGE (log_n > 16) or G3H_E_CUDA. */
+ * that device current); make that first call before any stream capture begins. Every call
+ * first enqueues three small kernels that check, on the GPU, whether the array holds the
+ * tables of this log_n, and rebuild them if it does not (the first call for a domain, or
+ * the first after a call for another domain, takes about a millisecond more). All calls
+ * on a device share the array and it keeps the last call's contents, so calls that overlap
+ * on the GPU (on different streams, or from different threads without ordering) race and
+ * give wrong results: order them on one stream.
+ * Returns G3H_OK, G3H_E_INVAL (a NULL pointer, or one not 16-byte aligned), G3H_E_RANGE
+ * (log_n > 16) or G3H_E_CUDA. */
 int g3h_compute_h_abc_static(uint32_t log_n, const uint32_t* a, const uint32_t* b,
                              const uint32_t* c, uint32_t* h_mont, uint32_t* h_std,
                              void* stream);
@@ -270,6 +274,19 @@ int g3h_timing_read(g3h_ctx* ctx, g3h_kernel_time* out, int max, int* count);
  * with CUDA events on the context's stream (best of three runs after a warm-up).
  * Synchronous. Returns G3H_E_INVAL (NULL), G3H_E_NOMEM or G3H_E_CUDA. */
 int g3h_measure_imad(g3h_ctx* ctx, double* results_per_s);
+
+/* The same probe for each kind of 32-bit integer multiply the field arithmetic issues:
+ * *per_s receives the thread-level instructions per second of independent chains of
+ *   G3H_MUL_LO:   mad.lo.u32   (the low word of a 32 x 32 product; = g3h_measure_imad)
+ *   G3H_MUL_HI:   mad.hi.u32   (the high word)
+ *   G3H_MUL_WIDE: mad.wide.u32 (the full 64-bit product, with a 64-bit addend)
+ * so that the cost of a full product can be stated in units of the 32-bit rate (the
+ * roofline's denominator) instead of assumed. Synchronous. Returns G3H_E_INVAL (NULL
+ * argument or unknown kind), G3H_E_NOMEM or G3H_E_CUDA. */
+#define G3H_MUL_LO 0
+#define G3H_MUL_HI 1
+#define G3H_MUL_WIDE 2
+int g3h_measure_int_mul(g3h_ctx* ctx, int kind, double* per_s);
 
 #ifdef __cplusplus
 }

@@ -123,7 +123,7 @@ def test_ntt_all_modes(log_n):
 @pytest.mark.parametrize("log_n", [19, 20, 21, 23])
 def test_ntt_large_and_three_levels(log_n):
     """2^19 and 2^20 run radix-4 pass pairs on 2^10 slices, 2^21 mixes 2^10 and 2^11
-    slices (radix-2 on the latter), 2^23 takes three levels."""
+    slices (the 256-thread radix-4 build on the latter), 2^23 takes three levels."""
     n = 1 << log_n
     x = synth.uniform_fr(synth.SplitMix64(200 + log_n), n)
     with g3h.Context(log_n) as ctx:
@@ -454,15 +454,15 @@ def test_timing_records_kernels():
         ctx.compute_h(w, hm, hs)
         t = ctx.timing_read()
         ctx.timing_enable(False)
-    # one stream per vector: two gathers (A, B), three launches per transform phase
-    assert {k: v[0] for k, v in t.items()} == {"gather": 2, "ntt_dif": 3, "ntt_mid": 3,
-                                               "ntt_dit": 3, "join": 1}
+    # one stream per vector: the gathers of A and of B, three launches per transform phase
+    assert {k: v[0] for k, v in t.items()} == {"gather_a": 1, "gather_b": 1, "ntt_dif": 3,
+                                               "ntt_mid": 3, "ntt_dit": 3, "join": 1}
     assert all(v[1] > 0 for v in t.values())
     with g3h.Context(log_n, w.shape[0], A, B) as ctx:
         ctx.timing_enable(True)
         hm2, hs2 = _zeros(n), _zeros(n)
         ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_SERIALIZE)
         t = ctx.timing_read()
-    assert {k: v[0] for k, v in t.items()} == {"gather": 2, "ntt_dif": 1, "ntt_mid": 1,
-                                               "ntt_dit": 1, "join": 1}
+    assert {k: v[0] for k, v in t.items()} == {"gather_a": 1, "gather_b": 1, "ntt_dif": 1,
+                                               "ntt_mid": 1, "ntt_dit": 1, "join": 1}
     assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
