@@ -54,6 +54,9 @@ def parse_args():
     p.add_argument("--msm-only", action="store_true",
                    help="time only the 2^18 H multiexp over G1 (the extra line's "
                         "measurement; for profiler captures of its kernels)")
+    p.add_argument("--stress-only", action="store_true",
+                   help="time only the 2^22 stress H on given a, b, c (the extra line's "
+                        "measurement; for profiler captures of its kernels)")
     p.add_argument("--serialize", action="store_true",
                    help="headline pass too with the three vectors in one launch per phase "
                         "on one stream (for profiler captures of the kernels as the "
@@ -353,6 +356,17 @@ def main():
     from bn254_scalar_field_gb300 import build, g3h, synth
 
     torch.cuda.set_device(local)
+    if args.stress_only:
+        build.build()
+        dev = torch.device("cuda", local)
+        r = stress_2_22(torch, dev, g3h, synth, reps=args.steps, warmup=args.warmup,
+                        flags=g3h.G3H_SERIALIZE if args.serialize else 0, extra=False)
+        if rank == 0:
+            print(json.dumps({"metric": "Groth16 H computations/s, 2^22 stress vectors",
+                              "value": r["h_2^22_per_s"], "unit": "H/s", "steps": args.steps,
+                              "warmup": args.warmup, "higher_is_better": True,
+                              "data": "synthetic", "extra": r}))
+        return
     if args.msm_only:
         build.build()
         dev = torch.device("cuda", local)
@@ -758,17 +772,40 @@ def other_domains(torch, dev, g3h, synth, flush, steps=200):
             flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
         ms = sum(a.elapsed_time(b) for a, b in evs) / steps
-        ctx.close()
+        ops = h_ops(k, int(A[0][-1]), int(B[0][-1]))
         out["h_per_s_2^%d" % k] = 1e3 / ms
         out["ms_per_h_2^%d" % k] = ms
-        ops = h_ops(k, int(A[0][-1]), int(B[0][-1]))
         out["h_2^%d_frac_of_derived_imad_peak" % k] = ops / (ms * 1e-3) / imad_peak()
+        # batched: many witnesses per call (device buffers), one launch per phase per
+        # chunk of witnesses on these domains
+        count = 256 if k <= 14 else 32
+        wb = wd.unsqueeze(0).repeat(count, 1, 1).contiguous()
+        hmb = torch.empty((count, n, 8), dtype=torch.int32, device=dev)
+        hsb = torch.empty_like(hmb)
+        for _ in range(2):
+            ctx.compute_h_batch(wb, hmb, hsb)
+        bms = []
+        for i in range(10):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ctx.compute_h_batch(wb, hmb, hsb)
+            e1.record(stream)
+            bms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        bms = statistics.median(a.elapsed_time(b) for a, b in bms)
+        out["batch_h_per_s_2^%d" % k] = count * 1e3 / bms
+        out["batch_count_2^%d" % k] = count
+        out["batch_h_2^%d_frac_of_derived_imad_peak" % k] = count * ops / (bms * 1e-3) / imad_peak()
+        ctx.close()
+        del wb, hmb, hsb
     return out
 
 
-def stress_2_22(torch, dev, g3h, synth):
+def stress_2_22(torch, dev, g3h, synth, reps=10, warmup=2, flags=0, extra=True):
     """Secondary figures on the 2^22 stress vectors (inputs larger than L2): one forward
-    coset NTT (Fr NTT Gelem/s) and the H path on given a, b, c = a*b."""
+    coset NTT (Fr NTT Gelem/s) and the H path on given a, b, c = a*b; with `extra` also the
+    witness copy to standard form on 2^24 elements."""
     k = synth.STRESS_LOG_N
     n = 1 << k
     a, b = synth.stress_ab(k)
@@ -781,10 +818,9 @@ def stress_2_22(torch, dev, g3h, synth):
     hs = torch.empty_like(ad)
     x = ad.clone()
     stream = torch.cuda.current_stream(dev)
-    reps = 10
 
     def timed(fn):
-        for _ in range(2):
+        for _ in range(warmup):
             fn()
         ts = []
         for _ in range(reps):
@@ -796,8 +832,14 @@ def stress_2_22(torch, dev, g3h, synth):
         torch.cuda.synchronize(dev)
         return statistics.median(a.elapsed_time(b) for a, b in ts)
 
+    h_ms = timed(lambda: ctx.compute_h_abc(ad, bd, cd, hm, hs, flags=flags))
+    if not extra:
+        ctx.sync()
+        ctx.close()
+        ops = h_ops(k, 0, 0, from_witness=False)
+        return {"h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
+                "h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / imad_peak()}
     ntt_ms = timed(lambda: ctx.ntt(x, coset=True))
-    h_ms = timed(lambda: ctx.compute_h_abc(ad, bd, cd, hm, hs))
     # the witness copy to standard form (HBM-bound: 32 bytes read + 32 written per
     # element) on 2^24 elements, 4x the L2 each way
     del x, hm, hs

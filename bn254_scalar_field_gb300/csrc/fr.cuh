@@ -105,9 +105,10 @@ __device__ __forceinline__ fr_t fr_zero() {
         "r"(a.v[6]), "r"(a.v[7]), "r"(bi))
 
 // a * b * 2^-256 mod r, inputs in [0, 2r), output in [0, 2r) (CIOS: one row per word of
-// b; written with even/odd carry chains because this GPU issues a 32x32 -> 64-bit product
-// at a quarter of the 32-bit multiply rate whether as one wide instruction or as a
-// low/high pair, and the chains above let the compiler issue each product once).
+// b; written with even/odd carry chains so that the low and high word of each product
+// sit in one chain and the compiler can issue the product once. Measured on GB300: a full
+// 32 x 32 -> 64-bit product costs about 2.7 of the 32-bit multiply-adds' issue slots on
+// the integer multiply pipe (mad.wide.u32 23.7 and mad.lo.u32 63.8 per clock per SM).
 __device__ __forceinline__ fr_t fr_mul(const fr_t& a, const fr_t& b) {
   uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0, t4 = 0, t5 = 0, t6 = 0, t7 = 0;
 #pragma unroll

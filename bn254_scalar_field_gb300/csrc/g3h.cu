@@ -189,6 +189,28 @@ void free_lane(Lane& l) {
   l = Lane();
 }
 
+// Batched H on small and middle domains: a chunk of up to `z` witnesses runs as one
+// launch per phase, the witness index in the grid's z dimension (slice kernels) or y
+// dimension (gather, join), so that a few thousand-point domains fill the GPU. Two such
+// lanes alternate between chunks, each with its own stream and buffers, so that one
+// chunk's copies (host-pointer calls) overlap the other's kernels.
+struct ZLane {
+  cudaStream_t stream = nullptr;
+  fr_t* ab_in = nullptr;  // z x 2n: the gathers' a | b per witness
+  fr_t* abc = nullptr;    // z x 3n: a | b | c per witness while they are transformed
+  fr_t* stage = nullptr;  // z x (n_wires + 2n): witnesses | h_mont | h_std (host pointers)
+  cudaEvent_t done = nullptr;
+};
+
+void free_zlane(ZLane& l) {
+  void* b[] = {l.ab_in, l.abc, l.stage};
+  for (void* x : b)
+    if (x) cudaFree(x);
+  if (l.done) cudaEventDestroy(l.done);
+  if (l.stream) cudaStreamDestroy(l.stream);
+  l = ZLane();
+}
+
 // The buffers of one group's multiexp (bytes as raw device memory, typed at use).
 struct MsmState {
   uint32_t n = 0;                    // bases prepared
@@ -242,6 +264,9 @@ struct g3h_ctx {
   };
   std::vector<Graph> graphs;
   std::vector<Lane> extra_lanes;  // batched calls: lanes 1, 2, ...
+  ZLane zl[2];                    // batched calls on small and middle domains
+  uint32_t z_chunk = 0;           // witnesses per chunk the z lanes hold (0: none yet)
+  bool z_staged = false;          // the z lanes hold staging buffers
   cudaEvent_t batch_start = nullptr;
   // multiexps over G1 and G2 (g3h_msm_prepare / g3h_msm and the _g2 pair)
   MsmState msm1, msm2;
@@ -286,6 +311,7 @@ void release(g3h_ctx* c) {
     if (b) cudaFree(b);
   for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
   for (Lane& l : c->extra_lanes) free_lane(l);
+  for (ZLane& l : c->zl) free_zlane(l);
   free_lane_streams(c->own);
   if (c->batch_start) cudaEventDestroy(c->batch_start);
   for (auto& g : c->graphs) cudaGraphExecDestroy(g.exec);
@@ -353,11 +379,18 @@ void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
   }
 }
 
+// Launches a slice kernel over the n >> kk slices of nvec vectors (grid rows) and nz
+// batch layers. With three vectors per launch, the three blocks of a slice are adjacent
+// in launch order (SliceArgs::vfast): they read the same twiddles and scale entries, which
+// then come from L2 for two of them.
 int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, Slice which,
-                    const SliceArgs& a, unsigned nvec) {
+                    const SliceArgs& a_in, unsigned nvec, unsigned nz = 1) {
   uint32_t threads = 0;
-  void (*kern)(SliceArgs) = slice_kernel(which, a.kk, &threads);
-  const dim3 grid((unsigned)(c->n >> a.kk), nvec);
+  void (*kern)(SliceArgs) = slice_kernel(which, a_in.kk, &threads);
+  SliceArgs a = a_in;
+  const unsigned slices = (unsigned)(c->n >> a.kk);
+  a.vfast = (nvec == 3u && !(a.mode & SL_JOIN)) ? 1u : 0u;
+  const dim3 grid(a.vfast ? 3u * slices : slices, a.vfast ? 1u : nvec, nz);
   const size_t smem = (size_t)32 << a.kk;
   return run_on(c, st, name, [&] { kern<<<grid, threads, smem, st>>>(a); });
 }
@@ -506,13 +539,13 @@ int quotient_vectors(g3h_ctx* c, const Lane& ln, const cudaStream_t* vs, bool se
     fr_t* ab = ln.ab_in;
     const uint32_t nn = (uint32_t)n;
     rc = run_on(c, vs[0], "gather_a", [&] {
-      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(c->d_rpa, c->d_cola, c->d_vala, w,
-                                                            c->n_rows_a, nn, ab, check, c->d_err);
+      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(
+          c->d_rpa, c->d_cola, c->d_vala, w, c->n_rows_a, nn, ab, check, c->d_err, 0, 0);
     });
     if (rc == G3H_OK)
       rc = run_on(c, vs[1], "gather_b", [&] {
         k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
-            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, ab + n, check, c->d_err);
+            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, ab + n, check, c->d_err, 0, 0);
       });
     if (rc != G3H_OK) return rc;
     if (!ok(cudaEventRecord(ln.ev_ga, vs[0])) || !ok(cudaEventRecord(ln.ev_gb, vs[1])) ||
@@ -623,7 +656,7 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
   NvtxRange range("g3h join");
   return run_on(c, st, "join", [&] {
     k_join<<<blocks_for(n, 256), 256, 0, st>>>(s_of(ln, n, 0), s_of(ln, n, 1), s_of(ln, n, 2), hm,
-                                                hs, n, 0u, c->d_err);
+                                                hs, n, 0u, c->d_err, 0, 0);
   });
 }
 
@@ -935,6 +968,151 @@ int g3h_compute_h_abc(g3h_ctx* c, const uint32_t* a, const uint32_t* b, const ui
 
 namespace {
 
+// Domains whose batched calls take the z lanes, and the chunk size: enough witnesses per
+// launch for about 2^20 elements per vector phase, at most 64.
+constexpr uint32_t kZMinLog = 6, kZMaxLog = 16;
+
+uint32_t z_chunk_for(uint32_t log_n) {
+  return std::min<uint32_t>(64u, std::max<uint32_t>(1u, (1u << 20) >> log_n));
+}
+
+int ensure_zlanes(g3h_ctx* c, bool staged) {
+  const uint32_t z = z_chunk_for(c->log_n);
+  if (c->z_chunk == z && (c->z_staged || !staged)) return G3H_OK;
+  const size_t n = c->n;
+  for (ZLane& l : c->zl) {
+    if (l.stream) cudaStreamSynchronize(l.stream);
+    free_zlane(l);
+  }
+  c->z_chunk = 0;
+  c->z_staged = false;
+  for (ZLane& l : c->zl) {
+    int rc = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) == cudaSuccess
+                 ? G3H_OK
+                 : G3H_E_CUDA;
+    if (rc == G3H_OK) rc = dalloc(&l.ab_in, (size_t)z * 2 * n);
+    if (rc == G3H_OK) rc = dalloc(&l.abc, (size_t)z * 3 * n);
+    if (rc == G3H_OK && staged) rc = dalloc(&l.stage, (size_t)z * (c->n_wires + 2 * n));
+    if (rc != G3H_OK) {
+      for (ZLane& m : c->zl) free_zlane(m);
+      return rc;
+    }
+  }
+  c->z_chunk = z;
+  c->z_staged = staged;
+  return G3H_OK;
+}
+
+// Steps 1-5 for nz witnesses at w + i * w_stride (device) -> h_mont, h_std at hm, hs +
+// i * h_stride (device), on a z lane: one launch per phase for all of them.
+int quotient_z(g3h_ctx* c, const ZLane& l, uint32_t nz, const fr_t* w, size_t w_stride,
+               fr_t* hm, fr_t* hs, size_t h_stride, uint32_t flags) {
+  const uint32_t k = c->log_n;
+  const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
+  const size_t n = c->n;
+  const cudaStream_t st = l.stream;
+  const uint32_t nn = (uint32_t)n;
+  const dim3 ggrid(blocks_for(n, 256), nz);
+  int rc = run_on(c, st, "gather_a", [&] {
+    k_gather_rows<<<ggrid, 256, 0, st>>>(c->d_rpa, c->d_cola, c->d_vala, w, c->n_rows_a, nn,
+                                         l.ab_in, check, c->d_err, w_stride, 2 * n);
+  });
+  if (rc == G3H_OK)
+    rc = run_on(c, st, "gather_b", [&] {
+      k_gather_rows<<<ggrid, 256, 0, st>>>(c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn,
+                                           l.ab_in + n, check, c->d_err, w_stride, 2 * n);
+    });
+  const Plan pl = plan_for(k);
+  fr_t* s[3] = {l.abc, l.abc + n, l.abc + 2 * n};
+  for (int lvl = pl.levels - 1; lvl >= 1 && rc == G3H_OK; lvl--) {
+    const bool first = lvl == pl.levels - 1;
+    SliceArgs x = base_args(c, flags);
+    x.src[0] = first ? l.ab_in : s[0];
+    x.src[1] = first ? l.ab_in + n : s[1];
+    x.src[2] = first ? nullptr : s[2];
+    for (int u = 0; u < 3; u++) x.dst[u] = s[u];
+    x.zs_src = first ? 2 * n : 3 * n;
+    x.zs_dst = 3 * n;
+    x.tw = c->d_tw_inv;
+    x.kk = pl.kk[lvl];
+    x.c0 = pl.c0[lvl];
+    x.mode = first ? SL_C_FROM_AB : 0u;
+    rc = launch_slice_on(c, st, "ntt_dif", Slice::dif, x, 3, nz);
+  }
+  if (rc == G3H_OK) {
+    SliceArgs x = base_args(c, flags);
+    for (int u = 0; u < 3; u++) x.dst[u] = s[u];
+    x.zs_dst = 3 * n;
+    x.tw = c->d_tw_inv;
+    x.tw2 = c->d_tw_fwd;
+    x.scale_tab = c->d_shift_br;
+    x.kk = pl.kk[0];
+    rc = launch_slice_on(c, st, "ntt_mid", Slice::mid, x, 3, nz);
+  }
+  for (int lvl = 1; lvl < pl.levels && rc == G3H_OK; lvl++) {
+    SliceArgs x = base_args(c, flags);
+    for (int u = 0; u < 3; u++) x.src[u] = x.dst[u] = s[u];
+    x.zs_src = x.zs_dst = 3 * n;
+    x.tw = c->d_tw_fwd;
+    x.kk = pl.kk[lvl];
+    x.c0 = pl.c0[lvl];
+    rc = launch_slice_on(c, st, "ntt_dit", Slice::dit, x, 3, nz);
+  }
+  if (rc == G3H_OK)
+    rc = run_on(c, st, "join", [&] {
+      k_join<<<dim3(blocks_for(n, 256), nz), 256, 0, st>>>(s[0], s[1], s[2], hm, hs, n, 0u,
+                                                           c->d_err, 3 * n, h_stride);
+    });
+  return rc;
+}
+
+// A batched call on the z lanes: chunks of up to z_chunk witnesses, alternating lanes.
+int batch_z(g3h_ctx* c, uint32_t count, const uint32_t* witnesses, uint32_t* h_mont,
+            uint32_t* h_std, uint32_t flags) {
+  const bool dev = (flags & G3H_DEVICE_PTRS) != 0u;
+  int rc = ensure_zlanes(c, !dev);
+  if (rc != G3H_OK) return rc;
+  const size_t n = c->n, nw = c->n_wires;
+  const uint32_t z = c->z_chunk;
+  // the lanes start after everything already queued on the context's stream
+  if (!c->batch_start &&
+      cudaEventCreateWithFlags(&c->batch_start, cudaEventDisableTiming) != cudaSuccess)
+    return G3H_E_CUDA;
+  if (cudaEventRecord(c->batch_start, c->stream) != cudaSuccess) return G3H_E_CUDA;
+  for (ZLane& l : c->zl)
+    if (cudaStreamWaitEvent(l.stream, c->batch_start, 0) != cudaSuccess) return G3H_E_CUDA;
+  uint32_t chunk = 0;
+  for (uint32_t i = 0; i < count && rc == G3H_OK; i += z, chunk++) {
+    const ZLane& l = c->zl[chunk & 1u];
+    const uint32_t nz = std::min(z, count - i);
+    const uint32_t* wi = witnesses + (size_t)i * 8 * nw;
+    uint32_t* hmi = h_mont + (size_t)i * 8 * n;
+    uint32_t* hsi = h_std + (size_t)i * 8 * n;
+    if (dev) {
+      rc = quotient_z(c, l, nz, (const fr_t*)wi, nw, (fr_t*)hmi, (fr_t*)hsi, n, flags);
+      continue;
+    }
+    fr_t* w = l.stage;
+    fr_t* hm = l.stage + (size_t)z * nw;
+    fr_t* hs = hm + (size_t)z * n;
+    rc = copy_on(l.stream, w, wi, (size_t)nz * nw * sizeof(fr_t), cudaMemcpyHostToDevice);
+    if (rc == G3H_OK) rc = quotient_z(c, l, nz, w, nw, hm, hs, n, flags);
+    if (rc == G3H_OK)
+      rc = copy_on(l.stream, hmi, hm, (size_t)nz * n * sizeof(fr_t), cudaMemcpyDeviceToHost);
+    if (rc == G3H_OK)
+      rc = copy_on(l.stream, hsi, hs, (size_t)nz * n * sizeof(fr_t), cudaMemcpyDeviceToHost);
+  }
+  // the context's stream waits for both lanes: the batch ends in its order
+  for (ZLane& l : c->zl)
+    if (cudaEventRecord(l.done, l.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(c->stream, l.done, 0) != cudaSuccess)
+      rc = G3H_E_CUDA;
+  if (dev) return rc;
+  const int rc2 = finish(c);
+  return rc != G3H_OK ? rc : rc2;
+}
+
 // Lanes of a batched call: the context's own plus up to kBatchLanes - 1 more, each with
 // its stream and buffers, allocated on first use and kept.
 constexpr uint32_t kBatchLanes = 3;
@@ -999,6 +1177,9 @@ int g3h_compute_h_batch(g3h_ctx* c, uint32_t count, const uint32_t* witnesses,
   NvtxRange range("g3h_compute_h_batch");
   const bool dev = (flags & G3H_DEVICE_PTRS) != 0u;
   if (dev && misaligned({witnesses, h_mont, h_std})) return G3H_E_INVAL;
+  if (c->log_n >= kZMinLog && c->log_n <= kZMaxLog && count > 1 &&
+      !(flags & G3H_FUSED_JOIN))
+    return batch_z(c, count, witnesses, h_mont, h_std, flags);
   const uint32_t lanes = std::min(count, kBatchLanes);
   int rc = ensure_lanes(c, lanes, !dev);
   if (rc != G3H_OK) return rc;
@@ -1087,7 +1268,8 @@ int g3h_join(g3h_ctx* c, const uint32_t* ea, const uint32_t* eb, const uint32_t*
   const uint32_t check = (flags & G3H_NOCHECK) ? 0u : 1u;
   auto launch = [&](const fr_t* x, const fr_t* y, const fr_t* z, fr_t* hm, fr_t* hs) {
     return run(c, "join", [&] {
-      k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(x, y, z, hm, hs, n, check, c->d_err);
+      k_join<<<blocks_for(n, 256), 256, 0, c->stream>>>(x, y, z, hm, hs, n, check, c->d_err, 0,
+                                                        0);
     });
   };
   if ((flags & G3H_DEVICE_PTRS) && misaligned({ea, eb, ec, h_mont, h_std})) return G3H_E_INVAL;

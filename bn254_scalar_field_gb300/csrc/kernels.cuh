@@ -9,7 +9,8 @@ namespace g3h {
 // Step 1, the sums of one matrix: thread i forms row i of A (or of B) against the
 // witness; the two matrices are launched separately, on separate streams, and c = a * b
 // is formed by the first inverse kernel of c at its load (SL_C_FROM_AB). Outputs
-// canonical. Launch: ceil(n / 256) blocks of 256.
+// canonical. Launch: ceil(n / 256) x (batch) blocks of 256; grid row blockIdx.y reads the
+// witness at w + blockIdx.y * w_stride and writes out + blockIdx.y * out_stride.
 //
 // The kernel lasts as long as its slowest warp, and a row is a chain of dependent loads
 // (column, witness value, coefficient) per term, so the longest row (95 terms in the
@@ -45,9 +46,12 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint32_t* __restrict_
                                                      const fr_t* __restrict__ val,
                                                      const fr_t* __restrict__ w,
                                                      uint32_t n_rows, uint32_t n, fr_t* out,
-                                                     uint32_t check, uint32_t* err) {
+                                                     uint32_t check, uint32_t* err,
+                                                     size_t w_stride, size_t out_stride) {
   // No early return: every lane takes part in the warp-wide loop below.
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  w += (size_t)blockIdx.y * w_stride;
+  out += (size_t)blockIdx.y * out_stride;
   const uint32_t lane = threadIdx.x & 31u;
   uint32_t kx = 0, ke = 0;
   if (i < n && i < n_rows) {
@@ -103,12 +107,20 @@ __global__ void __launch_bounds__(256) k_gather(const uint32_t* __restrict__ rpa
 }
 
 // Step 5 alone (POINTWISE_CU, g16_h_join): h = a*b - c in both encodings.
-// Launch: ceil(n / 256) blocks of 256.
+// Launch: ceil(n / 256) x (batch) blocks of 256; grid row blockIdx.y reads a, b, c +
+// blockIdx.y * in_stride and writes h_mont, h_std + blockIdx.y * h_stride.
 __global__ void __launch_bounds__(256) k_join(const fr_t* a, const fr_t* b, const fr_t* c,
                                               fr_t* h_mont, fr_t* h_std, size_t n,
-                                              uint32_t check, uint32_t* err) {
+                                              uint32_t check, uint32_t* err,
+                                              size_t in_stride, size_t h_stride) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  const size_t zi = (size_t)blockIdx.y * in_stride, zh = (size_t)blockIdx.y * h_stride;
+  a += zi;
+  b += zi;
+  c += zi;
+  h_mont += zh;
+  h_std += zh;
   const fr_t x = fr_load(a + i), y = fr_load(b + i), z = fr_load(c + i);
   if (check) {
     check_canonical(x, err);

@@ -48,7 +48,8 @@ enum : uint32_t {
   SL_C_FROM_AB = 16u,   // k_ntt_dif: vector 2 (c) is not loaded but formed as
                         // src[0][i] * src[1][i] (the gather's C = A o B) at load
   SL_JOIN_LAST = 32u,   // k_ntt_dit: vectors 0, 1, 2 (grid.y) are a, b, c; the last of a
-                        // slice's three blocks to finish writes h for that slice
+                        // slice's three blocks to finish writes h for that slice (one
+                        // problem per launch: the counters are per slice)
 };
 
 struct SliceArgs {
@@ -67,6 +68,13 @@ struct SliceArgs {
   uint32_t mode;   // SL_* flags
   uint32_t* counters;  // SL_JOIN_LAST: one zeroed counter per slice, left zeroed
   uint32_t vbase;      // vector of grid row blockIdx.y is vbase + blockIdx.y
+  uint32_t vfast;      // nonzero: the three vectors of a slice are adjacent blocks (slice
+                       // blockIdx.x / 3, vector vbase + blockIdx.x % 3; grid.y = 1), so that
+                       // they read the slice's twiddles and scales close together in time
+  // Batches: grid layer blockIdx.z works on an independent problem whose vectors are at
+  // src[v] + blockIdx.z * zs_src, dst[v] + blockIdx.z * zs_dst and h_mont / h_std +
+  // blockIdx.z * zs_h (elements; all zero for a single problem)
+  uint64_t zs_src, zs_dst, zs_h;
 };
 
 // 16-byte slot of element m's half: the low three bits (the bank group of a 16-byte
@@ -338,6 +346,14 @@ __device__ __forceinline__ size_t slice_base(uint32_t s, uint32_t c0, uint32_t k
   return (size_t)(s & ((1u << c0) - 1u)) + ((size_t)(s >> c0) << (c0 + kk));
 }
 
+// The slice and the vector (grid row) of this block, in either block order (SliceArgs::vfast).
+__device__ __forceinline__ uint32_t block_slice(const SliceArgs& p) {
+  return p.vfast ? blockIdx.x / 3u : blockIdx.x;
+}
+__device__ __forceinline__ uint32_t block_vector(const SliceArgs& p) {
+  return p.vbase + (p.vfast ? blockIdx.x % 3u : blockIdx.y);
+}
+
 // ---------------------------------------------------------------------------------------
 // k_ntt_dif: decimation-in-frequency passes over slice bits [c0, c0 + kk) of vector
 // vbase + blockIdx.y, src -> dst (in place when equal: every block reads its whole slice before
@@ -348,15 +364,17 @@ template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dif(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
-  const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
-  const size_t base = slice_base(blockIdx.x, c0, kk);
-  const uint32_t vec = p.vbase + blockIdx.y;
-  const fr_t* src = p.src[vec];
-  fr_t* dst = p.dst[vec];
+  const uint32_t sl = block_slice(p);
+  const uint32_t low = sl & ((1u << c0) - 1u);
+  const size_t base = slice_base(sl, c0, kk);
+  const uint32_t vec = block_vector(p);
+  const size_t zsrc = (size_t)blockIdx.z * p.zs_src;
+  const fr_t* src = p.src[vec] + zsrc;
+  fr_t* dst = p.dst[vec] + (size_t)blockIdx.z * p.zs_dst;
   const uint32_t check = p.mode & SL_CHECK;
   if ((p.mode & SL_C_FROM_AB) && vec == 2u) {
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
-      const size_t i = base + ((size_t)m << c0);
+      const size_t i = zsrc + base + ((size_t)m << c0);
       sm_put(sm, size, m, gather_c(fr_load(p.src[0] + i), fr_load(p.src[1] + i)));
     }
   } else {
@@ -383,8 +401,8 @@ template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_mid(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
-  const size_t base = (size_t)blockIdx.x << kk;
-  fr_t* vec = p.dst[p.vbase + blockIdx.y];
+  const size_t base = (size_t)block_slice(p) << kk;
+  fr_t* vec = p.dst[block_vector(p)] + (size_t)blockIdx.z * p.zs_dst;
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_load(vec + base + m));
   __syncthreads();
@@ -415,14 +433,17 @@ template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dit(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
-  const uint32_t low = blockIdx.x & ((1u << c0) - 1u);
-  const size_t base = slice_base(blockIdx.x, c0, kk);
+  const uint32_t sl = block_slice(p);
+  const uint32_t low = sl & ((1u << c0) - 1u);
+  const size_t base = slice_base(sl, c0, kk);
   const bool join = (p.mode & SL_JOIN) != 0u;
   const uint32_t nvec = join ? 3u : 1u;
+  const size_t zsrc = (size_t)blockIdx.z * p.zs_src, zdst = (size_t)blockIdx.z * p.zs_dst;
+  const size_t zh = (size_t)blockIdx.z * p.zs_h;
   for (uint32_t vi = 0; vi < nvec; vi++) {
-    const uint32_t v = join ? vi : p.vbase + blockIdx.y;
-    const fr_t* src = p.src[v];
-    fr_t* dst = p.dst[v];
+    const uint32_t v = join ? vi : block_vector(p);
+    const fr_t* src = p.src[v] + zsrc;
+    fr_t* dst = p.dst[v] + zdst;
     if (vi > 0) __syncthreads();  // the previous vector's last shared-memory reads
     for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
       sm_put(sm, size, m, fr_load(src + base + ((size_t)m << c0)));
@@ -432,11 +453,11 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
       const size_t i = base + ((size_t)m << c0);
       const fr_t x = sm_get(sm, size, m);
       if (join && v == 2u) {
-        const fr_t a = fr_load(p.dst[0] + i);
-        const fr_t b = fr_load(p.dst[1] + i);
+        const fr_t a = fr_load(p.dst[0] + zdst + i);
+        const fr_t b = fr_load(p.dst[1] + zdst + i);
         const fr_t h = fr_canon(fr_sub(fr_mul(a, b), x));
-        fr_store(p.h_mont + i, h);
-        fr_store(p.h_std + i, fr_from_mont(h));
+        fr_store(p.h_mont + zh + i, h);
+        fr_store(p.h_std + zh + i, fr_from_mont(h));
       } else if (join || (p.mode & SL_JOIN_LAST)) {
         fr_store(dst + i, x);
       } else {
@@ -452,20 +473,20 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      arrived = atomicAdd(p.counters + blockIdx.x, 1u);
+      arrived = atomicAdd(p.counters + sl, 1u);
       __threadfence();
     }
     __syncthreads();
     if (arrived == 2u) {
       for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
         const size_t i = base + ((size_t)m << c0);
-        const fr_t a = fr_ldcg(p.dst[0] + i), b = fr_ldcg(p.dst[1] + i);
-        const fr_t c = fr_ldcg(p.dst[2] + i);
+        const fr_t a = fr_ldcg(p.dst[0] + zdst + i), b = fr_ldcg(p.dst[1] + zdst + i);
+        const fr_t c = fr_ldcg(p.dst[2] + zdst + i);
         const fr_t h = fr_canon(fr_sub(fr_mul(a, b), c));
-        fr_store(p.h_mont + i, h);
-        fr_store(p.h_std + i, fr_from_mont(h));
+        fr_store(p.h_mont + zh + i, h);
+        fr_store(p.h_std + zh + i, fr_from_mont(h));
       }
-      if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;
+      if (threadIdx.x == 0) p.counters[sl] = 0u;
     }
   }
 }

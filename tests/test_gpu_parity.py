@@ -262,6 +262,42 @@ def test_compute_h_batch(log_n):
         assert g3h.lib().g3h_compute_h_batch(ctx.handle, 0, None, None, None, 0) == g3h.G3H_OK
 
 
+@pytest.mark.parametrize("log_n,count", [(6, 150), (14, 70), (16, 21)])
+def test_compute_h_batch_chunks(log_n, count):
+    """Batches on small and middle domains run one launch per phase for a chunk of
+    witnesses (64 at 2^6 and 2^14, 16 at 2^16), chunks alternating between two lanes:
+    several chunks, a ragged last one, every witness different, host and device memory,
+    and the same context's single-witness call after it."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    A, B, w0 = synth.problem(log_n, seed=900 + log_n)
+    n = 1 << log_n
+    nw = w0.shape[0]
+    ws = np.stack([w0] + [synth.witness(synth.SplitMix64(910 + i), nw, 0.9)
+                          for i in range(count - 1)])
+    with ThreadPoolExecutor(8) as ex:
+        want = list(ex.map(lambda i: oracle.compute_h(log_n, A, B, ws[i]), range(count)))
+    with g3h.Context(log_n, nw, A, B) as ctx:
+        hm = np.zeros((count, n, 8), np.uint32)
+        hs = np.zeros((count, n, 8), np.uint32)
+        ctx.compute_h_batch(ws, hm, hs)
+        for i in range(count):
+            assert np.array_equal(hm[i], want[i][0]) and np.array_equal(hs[i], want[i][1]), i
+        torch = _torch()
+        wd = torch.from_numpy(ws.view(np.int32)).cuda()
+        hmd = torch.zeros((count, n, 8), dtype=torch.int32, device="cuda")
+        hsd = torch.zeros((count, n, 8), dtype=torch.int32, device="cuda")
+        ctx.compute_h_batch(wd, hmd, hsd)
+        ctx.sync()
+        got_m, got_s = _host(hmd), _host(hsd)
+        for i in range(count):
+            assert np.array_equal(got_m[i], want[i][0]), i
+            assert np.array_equal(got_s[i], want[i][1]), i
+        h1m, h1s = _zeros(n), _zeros(n)
+        ctx.compute_h(ws[count - 1], h1m, h1s)
+        assert np.array_equal(h1m, want[-1][0]) and np.array_equal(h1s, want[-1][1])
+
+
 def test_compute_h_abc_stress_2_22():
     """The 2^22 NTT stress workload: a, b uniform, c = a*b, every element compared."""
     log_n = synth.STRESS_LOG_N
