@@ -55,8 +55,9 @@ def parse_args():
                    help="time only the 2^18 H multiexp over G1 (the extra line's "
                         "measurement; for profiler captures of its kernels)")
     p.add_argument("--stress-only", action="store_true",
-                   help="time only the 2^22 stress H on given a, b, c (the extra line's "
-                        "measurement; for profiler captures of its kernels)")
+                   help="time only the 2^22 stress H on given a, b, c and one 2^22 coset "
+                        "NTT (the extra line's measurements; for profiler captures of "
+                        "their kernels)")
     p.add_argument("--serialize", action="store_true",
                    help="headline pass too with the three vectors in one launch per phase "
                         "on one stream (for profiler captures of the kernels as the "
@@ -180,7 +181,7 @@ def launches_per_h(k, from_witness=True):
 def algorithmic_ops(kernel, k, nnz_a, nnz_b, from_witness=True):
     """Algorithmic 32-bit IMAD results of one launch of `kernel` (serialized H)."""
     ops = kernel_ops_per_h(k, nnz_a, nnz_b, from_witness)
-    if kernel not in ops:
+    if not ops.get(kernel):
         return 0
     return ops[kernel] // launches_per_h(k, from_witness)[kernel]
 
@@ -833,13 +834,14 @@ def stress_2_22(torch, dev, g3h, synth, reps=10, warmup=2, flags=0, extra=True):
         return statistics.median(a.elapsed_time(b) for a, b in ts)
 
     h_ms = timed(lambda: ctx.compute_h_abc(ad, bd, cd, hm, hs, flags=flags))
+    ntt_ms = timed(lambda: ctx.ntt(x, coset=True))
     if not extra:
         ctx.sync()
         ctx.close()
         ops = h_ops(k, 0, 0, from_witness=False)
         return {"h_2^22_abc_ms": h_ms, "h_2^22_per_s": 1e3 / h_ms,
-                "h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / imad_peak()}
-    ntt_ms = timed(lambda: ctx.ntt(x, coset=True))
+                "h_2^22_frac_of_derived_imad_peak": ops / (h_ms * 1e-3) / imad_peak(),
+                "ntt_2^22_coset_fwd_ms": ntt_ms, "ntt_2^22_gelem_s": n / (ntt_ms * 1e-3) / 1e9}
     # the witness copy to standard form (HBM-bound: 32 bytes read + 32 written per
     # element) on 2^24 elements, 4x the L2 each way
     del x, hm, hs

@@ -425,7 +425,8 @@ int build_table(g3h_ctx* c, fr_const_t* tab, size_t count, int base, int scale, 
   });
 }
 
-// The coset tables g^j and g^-j / n, allocated and built by the first coset transform.
+// The coset tables g^brev(p) (forward, at position p) and g^-j / n (inverse, at j),
+// allocated and built by the first coset transform.
 // They count as present only once both are allocated and their builds are enqueued; a
 // failure frees what was allocated, so the next call starts over.
 int ensure_coset_tables(g3h_ctx* c) {
@@ -433,7 +434,9 @@ int ensure_coset_tables(g3h_ctx* c) {
   int rc = G3H_OK;
   if (!c->d_coset_fwd) rc = dalloc(&c->d_coset_fwd, c->n);
   if (rc == G3H_OK && !c->d_coset_inv) rc = dalloc(&c->d_coset_inv, c->n);
-  if (rc == G3H_OK) rc = build_table(c, c->d_coset_fwd, c->n, 2, -1, 0);
+  // g^j stored at the bit-reversed position brev(j): the first kernel of a forward coset
+  // transform loads position p from data[brev(p)] and reads its scale contiguously
+  if (rc == G3H_OK) rc = build_table(c, c->d_coset_fwd, c->n, 2, -1, c->log_n);
   if (rc == G3H_OK) rc = build_table(c, c->d_coset_inv, c->n, 3, 4, 0);
   if (rc != G3H_OK) {
     cudaStreamSynchronize(c->stream);

@@ -222,8 +222,9 @@ __global__ void __launch_bounds__(32) k_small_quotient(const fr_t* a, const fr_t
 }
 
 // A natural-order transform of one small vector in place: position p loads
-// data[brev(p)] (times scale_load[brev(p)] if given), decimation-in-time passes with tw,
-// stores times scale_store[p] if given, else times kscale if given.
+// data[brev(p)] (times scale_load[p] if given: a table in bit-reversed order),
+// decimation-in-time passes with tw, stores times scale_store[p] if given, else times
+// kscale if given.
 // Launch: 1 block of 32 threads.
 __global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_const_t* tw,
                                                   const fr_const_t* scale_load,
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(32) k_small_ntt(fr_t* data, const fr_const_t* 
     const uint32_t j = bitrev(i, k);
     fr_t x = fr_load(data + j);
     if (check) check_canonical(x, err);
-    if (scale_load) x = fr_mul_c(x, scale_load[j]);
+    if (scale_load) x = fr_mul_c(x, scale_load[i]);
     s[i] = x;
   }
   __syncthreads();

@@ -294,24 +294,46 @@ __device__ __forceinline__ void dit_pass2(uint4* sm, uint32_t kk, const fr_const
   __syncthreads();
 }
 
-// All decimation-in-frequency passes of a slice (bits kk-1 .. 0), two at a time with R4.
+// The decimation-in-frequency passes of a slice on bits kk-1 .. lo_bit, two at a time with
+// R4.
 template <bool R4>
 __device__ __forceinline__ void dif_passes(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
-                                           uint32_t low, uint32_t c0, uint32_t k) {
+                                           uint32_t low, uint32_t c0, uint32_t k,
+                                           uint32_t lo_bit = 0) {
   int lb = (int)kk - 1;
   if (R4)
-    for (; lb >= 1; lb -= 2) dif_pass2(sm, kk, tw, (uint32_t)lb - 1u, low, c0, k);
-  for (; lb >= 0; lb--) dif_pass(sm, kk, tw, (uint32_t)lb, low, c0, k);
+    for (; lb >= (int)lo_bit + 1; lb -= 2) dif_pass2(sm, kk, tw, (uint32_t)lb - 1u, low, c0, k);
+  for (; lb >= (int)lo_bit; lb--) dif_pass(sm, kk, tw, (uint32_t)lb, low, c0, k);
 }
 
-// All decimation-in-time passes of a slice (bits 0 .. kk-1), two at a time with R4.
+// The decimation-in-time passes of a slice on bits first_bit .. kk-1, two at a time with R4.
 template <bool R4>
 __device__ __forceinline__ void dit_passes(uint4* sm, uint32_t kk, const fr_const_t* __restrict__ tw,
-                                           uint32_t low, uint32_t c0, uint32_t k) {
-  uint32_t lb = 0;
+                                           uint32_t low, uint32_t c0, uint32_t k,
+                                           uint32_t first_bit = 0) {
+  uint32_t lb = first_bit;
   if (R4)
     for (; lb + 1u < kk; lb += 2) dit_pass2(sm, kk, tw, lb, low, c0, k);
   for (; lb < kk; lb++) dit_pass(sm, kk, tw, lb, low, c0, k);
+}
+
+// On a contiguous slice (c0 = 0): the inverse's pass on bit 0 (twiddle 1), the coset shift
+// and the forward's pass on bit 0 (twiddle 1). All three work on the element pairs
+// (2m, 2m + 1), so one thread holds each pair throughout: (u, v) -> (u + v, u - v), times
+// the shift entries (s_2m, s_2m+1) -> (a, b) -> (a + b, a - b); then a barrier.
+__device__ __forceinline__ void bit0_shift_bit0(uint4* sm, uint32_t kk,
+                                                const fr_const_t* __restrict__ shift) {
+  const uint32_t size = 1u << kk;
+#pragma unroll 1
+  for (uint32_t bf = threadIdx.x; bf < (size >> 1); bf += blockDim.x) {
+    const uint32_t lo = 2u * bf, hi = lo + 1u;
+    const fr_t u = sm_get(sm, size, lo), v = sm_get(sm, size, hi);
+    const fr_t a = fr_mul_c(fr_add(u, v), fr_const_ldg(shift + lo));
+    const fr_t b = fr_mul_c(fr_sub(u, v), fr_const_ldg(shift + hi));
+    sm_put(sm, size, lo, fr_add(a, b));
+    sm_put(sm, size, hi, fr_sub(a, b));
+  }
+  __syncthreads();
 }
 
 // Three builds of each slice kernel, chosen by slice size (measured on GB300):
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 // vector vbase + blockIdx.y: the inverse transform's decimation-in-frequency passes on bits
 // kk-1 .. 0 (twiddles p.tw), the shift by scale_tab[position] (g^brev(position) / n),
 // then the forward transform's decimation-in-time passes on bits 0 .. kk-1 (twiddles
-// p.tw2). In place. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
+// p.tw2). In place. With kk odd the two passes on bit 0 and the shift run as one step. Launch: grid (n >> kk, vectors), block min(2^(kk-1), 256), shared
 // 2^kk * 32 bytes.
 template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_mid(const __grid_constant__ SliceArgs p) {
@@ -406,11 +428,19 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     sm_put(sm, size, m, fr_load(vec + base + m));
   __syncthreads();
-  dif_passes<SliceCfg<C>::r4>(sm, kk, p.tw, 0u, 0u, k);
-  for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
-    sm_put(sm, size, m, fr_mul_c(sm_get(sm, size, m), fr_const_ldg(p.scale_tab + base + m)));
-  __syncthreads();
-  dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw2, 0u, 0u, k);
+  if (kk & 1u) {
+    // odd slice bits: the passes on bit 0 meet the shift in one step (two barriers and two
+    // shared-memory round trips fewer); the forward's pairs then start at bit 1
+    dif_passes<SliceCfg<C>::r4>(sm, kk, p.tw, 0u, 0u, k, 1u);
+    bit0_shift_bit0(sm, kk, p.scale_tab + base);
+    dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw2, 0u, 0u, k, 1u);
+  } else {
+    dif_passes<SliceCfg<C>::r4>(sm, kk, p.tw, 0u, 0u, k);
+    for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
+      sm_put(sm, size, m, fr_mul_c(sm_get(sm, size, m), fr_const_ldg(p.scale_tab + base + m)));
+    __syncthreads();
+    dit_passes<SliceCfg<C>::r4>(sm, kk, p.tw2, 0u, 0u, k);
+  }
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x)
     fr_store(vec + base + m, sm_get(sm, size, m));
 }
@@ -495,7 +525,8 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 // k_ntt_brev: the first decimation-in-time passes (bits 0 .. kk-1) of a natural-order
 // transform, on the contiguous slice at blockIdx.x << kk: position i loads src[brev(i)]
 // (the bit-reversal permutation absorbed into the load, as on the NTT_CU page), scaled by
-// scale_tab[brev(i)] (SL_SCALE_TABLE) or kscale (SL_SCALE_CONST), and the result goes to
+// scale_tab[i] (SL_SCALE_TABLE: a table kept in bit-reversed order, so that its reads are
+// contiguous) or kscale (SL_SCALE_CONST), and the result goes to
 // dst (out of place: a block reads other blocks' elements). The passes are those of the
 // slice build C (radix-4 pass pairs in builds 1 and 2). Every 32-byte element is one
 // sector, so the scattered loads read no byte they do not use.
@@ -509,7 +540,7 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
     const uint32_t j = bitrev((uint32_t)base + m, k);
     fr_t x = fr_load(p.src[0] + j);
     if (p.mode & SL_CHECK) check_canonical(x, p.err);
-    if (p.mode & SL_SCALE_TABLE) x = fr_mul_c(x, fr_const_ldg(p.scale_tab + j));
+    if (p.mode & SL_SCALE_TABLE) x = fr_mul_c(x, fr_const_ldg(p.scale_tab + base + m));
     if (p.mode & SL_SCALE_CONST) x = fr_mul_c(x, p.kscale);
     sm_put(sm, size, m, x);
   }

@@ -93,7 +93,8 @@ def test_injected_launch_and_copy_errors_leave_the_context_usable(log_n, points)
     with g3h.Context(log_n, w.shape[0], A, B) as ctx:
         # the launches and copies of a host-pointer call each fail in turn (2^4: witness
         # copy, gather, one-block quotient, two result copies; 2^10: the copy, then the
-        # launches captured into the launch graph)
+        # launches captured into the launch graph: two gathers, three per transform phase,
+        # the join)
         for i in range(1, points + 1):
             with _Fault("cuda:%d" % i):
                 rc = _code(lambda: _h(ctx, w, n))
