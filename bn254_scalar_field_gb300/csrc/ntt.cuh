@@ -544,7 +544,10 @@ template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_brev(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
-  const size_t base = (size_t)blockIdx.x << kk;
+  // Block b runs slice brev(b): slice s reads the elements whose low k - kk index bits are
+  // brev(s), so consecutive blocks read neighbouring elements, which share cache lines
+  // (measured at 2^22: 805 -> 403 MB of DRAM reads per launch, 439 -> 428 us)
+  const size_t base = (size_t)bitrev(blockIdx.x, k - kk) << kk;
   for (uint32_t m = threadIdx.x; m < size; m += blockDim.x) {
     const uint32_t j = bitrev((uint32_t)base + m, k);
     fr_t x = fr_load(p.src[0] + j);
