@@ -13,9 +13,13 @@
 // captured once into a CUDA graph per set of pointers and replayed; G3H_SERIALIZE runs the
 // three vectors as one launch per phase on one stream, G3H_FUSED_JOIN writes h from the last
 // forward kernel instead of k_join. Slice kernels come in three builds (ntt.cuh, SliceCfg):
-// radix-4 pass pairs for slices of 2^9 elements and more, radix-2 passes below.
+// radix-4 pass pairs for slices of 2^9 elements and more, radix-2 passes below. Batched
+// calls on domains of 2^6 .. 2^16 points run a chunk of witnesses per launch (the witness
+// index in the grid's z or y dimension) on two alternating "z lanes".
 //
 // The multiexps over G1 and G2 (msm.cuh) keep their prepared bases in the context.
+// Every computing entry point and every stage of an H is an NVTX range; the environment
+// variable G3H_FAULT injects allocation or launch failures on the host (inject_fault).
 #include <cuda_runtime.h>
 
 #include <nvtx3/nvToolsExt.h>

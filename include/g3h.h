@@ -43,6 +43,12 @@
  *
  * Threads. A context may be used by one host thread at a time; calls on one context run
  * in order on its stream. Separate contexts are independent.
+ *
+ * Failure injection, for tests of the failure paths (nothing is done to the GPU): with the
+ * environment variable G3H_FAULT set to "alloc:N" the N-th device or pinned allocation the
+ * library attempts fails as if out of memory (G3H_E_NOMEM); with "cuda:N" the N-th kernel
+ * launch or copy is not issued and reports G3H_E_CUDA. N counts from 1 and restarts when
+ * the value changes; unset, empty or malformed: no effect.
  */
 #ifndef G3H_H
 #define G3H_H
