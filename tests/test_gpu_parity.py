@@ -298,6 +298,35 @@ def test_compute_h_batch_chunks(log_n, count):
         assert np.array_equal(h1m, want[-1][0]) and np.array_equal(h1s, want[-1][1])
 
 
+def test_compute_h_batch_reports_a_noncanonical_witness():
+    """A batch on the z lanes with one witness holding a value >= r: the call reports
+    G3H_E_NONCANON (host buffers) or the next sync does (device buffers), and the context
+    computes bit-exact results afterwards."""
+    log_n = 10
+    n = 1 << log_n
+    A, B, w = synth.problem(log_n, seed=950)
+    ws = np.stack([w] * 5)
+    ws[3, :] = synth.MODULUS_LIMBS  # every wire of witness 3 (the gathers read some)
+    want_m, want_s = oracle.compute_h(log_n, A, B, w)
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        hm = np.zeros((5, n, 8), np.uint32)
+        hs = np.zeros((5, n, 8), np.uint32)
+        with pytest.raises(g3h.G3HError) as ei:
+            ctx.compute_h_batch(ws, hm, hs)
+        assert ei.value.code == g3h.G3H_E_NONCANON
+        torch = _torch()
+        ctx.compute_h_batch(torch.from_numpy(ws.view(np.int32)).cuda(),
+                            torch.zeros((5, n, 8), dtype=torch.int32, device="cuda"),
+                            torch.zeros((5, n, 8), dtype=torch.int32, device="cuda"))
+        with pytest.raises(g3h.G3HError) as ei:
+            ctx.sync()
+        assert ei.value.code == g3h.G3H_E_NONCANON
+        good = np.stack([w] * 5)
+        ctx.compute_h_batch(good, hm, hs)
+        for i in range(5):
+            assert np.array_equal(hm[i], want_m) and np.array_equal(hs[i], want_s), i
+
+
 def test_compute_h_abc_stress_2_22():
     """The 2^22 NTT stress workload: a, b uniform, c = a*b, every element compared."""
     log_n = synth.STRESS_LOG_N
