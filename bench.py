@@ -143,8 +143,8 @@ def kernel_counts_per_h(k, nnz_a, nnz_b, from_witness=True):
     reductions)}. gather_a / gather_b: one multiply per term of A / of B; ntt_dif: the
     butterflies of the inverse's top slice levels (3 vectors) and, from a witness, the n
     products c = a * b formed at its load; ntt_mid: the low levels of both transforms, the
-    1/n scale and the coset shift (3 vectors); ntt_dit: the forward's top levels; join: n
-    products a * b and the n reductions of h_std."""
+    1/n scale and the coset shift (3 vectors); ntt_dit: the forward's top levels; prejoin:
+    the join's n products a * b; join: the n reductions of h_std."""
     n = 1 << k
     kk = plan_for(k)
     top = sum(kk[1:])
@@ -155,7 +155,8 @@ def kernel_counts_per_h(k, nnz_a, nnz_b, from_witness=True):
     c["ntt_dif"] = (3 * top * (n // 2) + (n if from_witness else 0), 0)
     c["ntt_mid"] = (3 * (kk[0] * n + 2 * n), 0)
     c["ntt_dit"] = (3 * top * (n // 2), 0)
-    c["join"] = (n, n)
+    c["prejoin"] = (n, 0)
+    c["join"] = (0, n)
     return c
 
 
@@ -172,7 +173,7 @@ def kernel_ops_per_h(k, nnz_a, nnz_b, from_witness=True, mm_ops=None, red_ops=No
 def launches_per_h(k, from_witness=True):
     """Launches per kernel name of one H with G3H_SERIALIZE (three vectors per launch)."""
     levels = len(plan_for(k))
-    out = {"ntt_dif": levels - 1, "ntt_mid": 1, "ntt_dit": levels - 1, "join": 1}
+    out = {"ntt_dif": levels - 1, "ntt_mid": 1, "ntt_dit": levels - 1, "prejoin": 1, "join": 1}
     if from_witness:
         out.update({"gather_a": 1, "gather_b": 1})
     return out

@@ -160,6 +160,7 @@ struct Lane {
                                // be the legacy default stream, which cannot be captured)
   cudaEvent_t ev_fork = nullptr, ev_ga = nullptr, ev_gb = nullptr;
   cudaEvent_t ev_end[2] = {nullptr, nullptr};
+  cudaEvent_t ev_a = nullptr, ev_p = nullptr;  // vector a transformed; the join's product formed
 };
 
 int make_lane_streams(Lane& l) {
@@ -167,7 +168,8 @@ int make_lane_streams(Lane& l) {
     if (cudaStreamCreateWithFlags(&l.aux[i], cudaStreamNonBlocking) != cudaSuccess)
       return G3H_E_CUDA;
   if (cudaStreamCreateWithFlags(&l.cap, cudaStreamNonBlocking) != cudaSuccess) return G3H_E_CUDA;
-  cudaEvent_t* evs[] = {&l.ev_fork, &l.ev_ga, &l.ev_gb, &l.ev_end[0], &l.ev_end[1]};
+  cudaEvent_t* evs[] = {&l.ev_fork, &l.ev_ga,     &l.ev_gb, &l.ev_end[0],
+                        &l.ev_end[1], &l.ev_a, &l.ev_p};
   for (cudaEvent_t* e : evs)
     if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return G3H_E_CUDA;
   return G3H_OK;
@@ -177,7 +179,7 @@ void free_lane_streams(Lane& l) {
   for (int i = 0; i < 2; i++)
     if (l.aux[i]) cudaStreamDestroy(l.aux[i]);
   if (l.cap) cudaStreamDestroy(l.cap);
-  cudaEvent_t evs[] = {l.ev_fork, l.ev_ga, l.ev_gb, l.ev_end[0], l.ev_end[1]};
+  cudaEvent_t evs[] = {l.ev_fork, l.ev_ga, l.ev_gb, l.ev_end[0], l.ev_end[1], l.ev_a, l.ev_p};
   for (cudaEvent_t e : evs)
     if (e) cudaEventDestroy(e);
 }
@@ -653,18 +655,35 @@ int quotient_launches(g3h_ctx* c, const Lane& ln, const fr_t* a, const fr_t* b,
                   !ok(cudaStreamWaitEvent(vs[2], ln.ev_fork, 0))))
     return G3H_E_CUDA;
   int rc = quotient_vectors(c, ln, vs, serial, a, b, cc, w, hm, hs, flags);
-  // join: the lane's stream waits for vectors b and c
+  if (rc == G3H_OK && !(flags & G3H_FUSED_JOIN)) {
+    // The join in two steps. The product p = a * b needs only vectors a and b, which are
+    // done well before c (its chain starts once both gathers are done), so it is formed
+    // on b's stream, over a, while c's last kernel still runs; the join then reduces on
+    // c's stream, right after c's last kernel: h = p - c and its standard form.
+    NvtxRange range("g3h join");
+    fr_t* p = s_of(ln, n, 0);
+    if (!serial && (!ok(cudaEventRecord(ln.ev_a, vs[0])) ||
+                    !ok(cudaStreamWaitEvent(vs[1], ln.ev_a, 0))))
+      rc = G3H_E_CUDA;
+    if (rc == G3H_OK)
+      rc = run_on(c, vs[1], "prejoin", [&] {
+        k_join_product<<<blocks_for(n, 256), 256, 0, vs[1]>>>(p, s_of(ln, n, 1), n);
+      });
+    if (rc == G3H_OK && !serial &&
+        (!ok(cudaEventRecord(ln.ev_p, vs[1])) || !ok(cudaStreamWaitEvent(vs[2], ln.ev_p, 0))))
+      rc = G3H_E_CUDA;
+    if (rc == G3H_OK)
+      rc = run_on(c, vs[2], "join", [&] {
+        k_join_reduce<<<blocks_for(n, 256), 256, 0, vs[2]>>>(p, s_of(ln, n, 2), hm, hs, n);
+      });
+  }
+  // the lane's stream waits for streams b and c, also after a failed launch
   if (!serial)
     for (int i = 0; i < 2; i++)
       if (!ok(cudaEventRecord(ln.ev_end[i], vs[i + 1])) ||
           !ok(cudaStreamWaitEvent(st, ln.ev_end[i], 0)))
         rc = G3H_E_CUDA;
-  if (rc != G3H_OK || (flags & G3H_FUSED_JOIN)) return rc;
-  NvtxRange range("g3h join");
-  return run_on(c, st, "join", [&] {
-    k_join<<<blocks_for(n, 256), 256, 0, st>>>(s_of(ln, n, 0), s_of(ln, n, 1), s_of(ln, n, 2), hm,
-                                                hs, n, 0u, c->d_err, 0, 0);
-  });
+  return rc;
 }
 
 // quotient_launches through a launch graph: captured on the first call with a given lane,

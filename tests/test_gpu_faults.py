@@ -85,7 +85,7 @@ def test_prepare_fails_cleanly_at_every_allocation():
     del n
 
 
-@pytest.mark.parametrize("log_n,points", [(4, 5), (10, 12)])
+@pytest.mark.parametrize("log_n,points", [(4, 5), (10, 14)])
 def test_injected_launch_and_copy_errors_leave_the_context_usable(log_n, points):
     n = 1 << log_n
     A, B, w = synth.problem(log_n, seed=79)
@@ -94,7 +94,7 @@ def test_injected_launch_and_copy_errors_leave_the_context_usable(log_n, points)
         # the launches and copies of a host-pointer call each fail in turn (2^4: witness
         # copy, gather, one-block quotient, two result copies; 2^10: the copy, then the
         # launches captured into the launch graph: two gathers, three per transform phase,
-        # the join)
+        # the join's product and its reduction)
         for i in range(1, points + 1):
             with _Fault("cuda:%d" % i):
                 rc = _code(lambda: _h(ctx, w, n))

@@ -519,9 +519,11 @@ def test_timing_records_kernels():
         ctx.compute_h(w, hm, hs)
         t = ctx.timing_read()
         ctx.timing_enable(False)
-    # one stream per vector: the gathers of A and of B, three launches per transform phase
+    # one stream per vector: the gathers of A and of B, three launches per transform phase,
+    # the join's product and its reduction
     assert {k: v[0] for k, v in t.items()} == {"gather_a": 1, "gather_b": 1, "ntt_dif": 3,
-                                               "ntt_mid": 3, "ntt_dit": 3, "join": 1}
+                                               "ntt_mid": 3, "ntt_dit": 3, "prejoin": 1,
+                                               "join": 1}
     assert all(v[1] > 0 for v in t.values())
     with g3h.Context(log_n, w.shape[0], A, B) as ctx:
         ctx.timing_enable(True)
@@ -529,5 +531,6 @@ def test_timing_records_kernels():
         ctx.compute_h(w, hm2, hs2, flags=g3h.G3H_SERIALIZE)
         t = ctx.timing_read()
     assert {k: v[0] for k, v in t.items()} == {"gather_a": 1, "gather_b": 1, "ntt_dif": 1,
-                                               "ntt_mid": 1, "ntt_dit": 1, "join": 1}
+                                               "ntt_mid": 1, "ntt_dit": 1, "prejoin": 1,
+                                               "join": 1}
     assert np.array_equal(hm2, hm) and np.array_equal(hs2, hs)
