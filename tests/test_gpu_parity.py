@@ -228,6 +228,31 @@ def test_compute_h_proving_key_configs(log_n):
             assert np.array_equal(_host(hsd), want_s)
 
 
+@pytest.mark.parametrize("max_len", [8, 9, 200])
+def test_compute_h_row_lengths(max_len):
+    """Rows of at most 8 terms are summed a lane each and longer ones by the whole warp:
+    matrices whose rows stop at exactly 8 terms (every row a lane's), at 9, and reach 200,
+    through the single and the batched path, against the oracle."""
+    log_n = 10
+    n = 1 << log_n
+    A, B, w = synth.problem(log_n, seed=800 + max_len, max_a=max_len, max_b=max_len)
+    lens = np.diff(np.asarray(B[0], np.int64))
+    assert lens.max() == max_len or max_len == 200
+    want_m, want_s = oracle.compute_h(log_n, A, B, w)
+    ws = np.stack([w, synth.witness(synth.SplitMix64(900 + max_len), w.shape[0], 0.5)])
+    want2 = oracle.compute_h(log_n, A, B, ws[1])
+    with g3h.Context(log_n, w.shape[0], A, B) as ctx:
+        for fl in (0, g3h.G3H_SERIALIZE):
+            hm, hs = _zeros(n), _zeros(n)
+            ctx.compute_h(w, hm, hs, flags=fl)
+            assert np.array_equal(hm, want_m) and np.array_equal(hs, want_s), fl
+        hm = np.zeros((2, n, 8), np.uint32)
+        hs = np.zeros((2, n, 8), np.uint32)
+        ctx.compute_h_batch(ws, hm, hs)
+        assert np.array_equal(hm[0], want_m) and np.array_equal(hs[0], want_s)
+        assert np.array_equal(hm[1], want2[0]) and np.array_equal(hs[1], want2[1])
+
+
 @pytest.mark.parametrize("log_n", [4, 12, 14])
 def test_compute_h_batch(log_n):
     """Batched H (several witnesses, one prepared context): every witness's output equals
