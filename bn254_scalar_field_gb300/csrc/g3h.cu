@@ -392,12 +392,14 @@ void (*slice_kernel(Slice which, uint32_t kk, uint32_t* threads))(SliceArgs) {
 // in launch order (SliceArgs::vfast): they read the same twiddles and scale entries, which
 // then come from L2 for two of them.
 //
-// Launches on slices of at most 2^9 elements ask for the split of the SM's L1 / shared
-// memory that holds just the shared memory of as many blocks as can be resident, the rest
-// left to L1, where the twiddle and shift loads hit: 2^18 H 0.2783 -> 0.2775 ms (one fixed
-// 40 % of the maximum for all slice kernels: 0.2811 -> 0.2798; all of it: 0.2870). For the
-// larger slices the same rule measured slower (2^19 H 0.504 -> 0.513 ms, 2^22 4.63 -> 4.87),
-// so they keep the driver's choice.
+// On domains whose slices are all of at most 2^9 elements (2^18 and below), each launch
+// asks for the split of the SM's L1 / shared memory that holds just the shared memory of as
+// many blocks as can be resident, the rest left to L1, where the twiddle and shift loads
+// hit: 2^18 H 0.2783 -> 0.2775 ms (one fixed 40 % of the maximum for all slice kernels:
+// 0.2811 -> 0.2798; all of it: 0.2870). With larger slices the same rule measured slower
+// (2^22 H 4.63 -> 4.87 ms), and so did asking it only for a domain's 2^9 slices while its
+// 2^10 slices ran beside them with the driver's split (2^19 H 0.504 -> 0.513 ms): such
+// domains keep the driver's choice for every launch.
 constexpr uint32_t kCarveoutMaxSliceBits = 9;
 
 int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, Slice which,
@@ -409,8 +411,10 @@ int launch_slice_on(g3h_ctx* c, cudaStream_t st, const char* name, Slice which,
   a.vfast = (nvec == 3u && !(a.mode & SL_JOIN)) ? 1u : 0u;
   const dim3 grid(a.vfast ? 3u * slices : slices, a.vfast ? 1u : nvec, nz);
   const size_t smem = (size_t)32 << a.kk;
-  if (a.kk > kCarveoutMaxSliceBits)
-    return run_on(c, st, name, [&] { kern<<<grid, threads, smem, st>>>(a); });
+  const Plan pl = plan_for(c->log_n);
+  bool carve = true;
+  for (int l = 0; l < pl.levels; l++) carve = carve && pl.kk[l] <= kCarveoutMaxSliceBits;
+  if (!carve) return run_on(c, st, name, [&] { kern<<<grid, threads, smem, st>>>(a); });
   int8_t& pct = c->carveout[(int)which][a.kk & 31u];
   if (pct == 0) {
     int resident = 0;
