@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(256) k_join(const fr_t* a, const fr_t* b, cons
 // writes it). k_join_reduce: h = p - c in Montgomery form and from_mont(h), the same
 // values as k_join. Launch: ceil(n / 256) blocks of 256.
 __global__ void __launch_bounds__(256) k_join_product(fr_t* a, const fr_t* b, size_t n) {
+  wait_prior_grid();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   fr_store(a + i, fr_canon(fr_mul(fr_load(a + i), fr_load(b + i))));
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(256) k_join_product(fr_t* a, const fr_t* b, si
 
 __global__ void __launch_bounds__(256) k_join_reduce(const fr_t* p, const fr_t* c, fr_t* h_mont,
                                                      fr_t* h_std, size_t n) {
+  wait_prior_grid();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const fr_t h = fr_canon(fr_sub(fr_load(p + i), fr_load(c + i)));

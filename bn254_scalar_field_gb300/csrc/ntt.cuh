@@ -99,6 +99,13 @@ __device__ __forceinline__ fr_t sm_get(const uint4* sm, uint32_t half, uint32_t 
   return a;
 }
 
+// In a launch made with programmatic stream serialization: waits until the previous kernel
+// on the stream has completed and its writes are visible (the grid may have been launched
+// while that kernel's last blocks ran); in any other launch it returns at once.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t bitrev(uint32_t x, uint32_t bits) {
   return bits == 0u ? 0u : (__brev(x) >> (32u - bits));
 }
@@ -394,6 +401,7 @@ __device__ __forceinline__ uint32_t block_vector(const SliceArgs& p) {
 template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dif(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
+  wait_prior_grid();
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t sl = block_slice(p);
   const uint32_t low = sl & ((1u << c0) - 1u);
@@ -431,6 +439,7 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_mid(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
+  wait_prior_grid();
   const uint32_t kk = p.kk, k = p.log_n, size = 1u << kk;
   const size_t base = (size_t)block_slice(p) << kk;
   fr_t* vec = p.dst[block_vector(p)] + (size_t)blockIdx.z * p.zs_dst;
@@ -471,6 +480,7 @@ __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks)
 template <int C>
 __global__ void __launch_bounds__(SliceCfg<C>::threads, SliceCfg<C>::min_blocks) k_ntt_dit(const __grid_constant__ SliceArgs p) {
   extern __shared__ uint4 sm[];
+  wait_prior_grid();
   const uint32_t kk = p.kk, c0 = p.c0, k = p.log_n, size = 1u << kk;
   const uint32_t sl = block_slice(p);
   const uint32_t low = sl & ((1u << c0) - 1u);
