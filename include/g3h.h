@@ -75,12 +75,13 @@ extern "C" {
 #define G3H_NOCHECK 0x2u      /* skip the canonical-input checks */
 #define G3H_FUSED_JOIN 0x4u   /* compute_h / compute_h_abc: write h from the last forward
                                  kernel (the last of a slice's three blocks to finish
-                                 joins that slice) instead of finishing the three forward
-                                 transforms and running the standalone join kernel
-                                 (POINTWISE_CU, g16_h_join). The pages fuse to save a read
-                                 of a, b, c; on GB300 these kernels are bound by the
-                                 integer multiplier and the standalone join measured
-                                 faster, so it is the default. Same results. */
+                                 joins that slice) instead of the join's own kernels after
+                                 the forward transforms (POINTWISE_CU, g16_h_join): the
+                                 product a * b once a and b are transformed, the reduction
+                                 h = p - c once c is. The pages fuse to save a read of
+                                 a, b, c; on GB300 these kernels are bound by the integer
+                                 multiplier and the separate join measured faster, so it
+                                 is the default. Same results. */
 
 #define G3H_SERIALIZE 0x8u    /* compute_h / compute_h_abc: run the three vectors' transforms
                                  as one launch per phase on the context's stream instead
@@ -266,7 +267,11 @@ int g3h_timing_enable(g3h_ctx* ctx, int enable);
 
 /* Aggregates the recorded launches per kernel name after waiting for the stream: up to
  * `max` entries (name, number of launches, summed device milliseconds); *count receives
- * the number of distinct kernels. Names are static strings. */
+ * the number of distinct kernels. Names are static strings; an H records "gather_a",
+ * "gather_b", "ntt_dif", "ntt_mid", "ntt_dit", "prejoin" (the join's products) and "join"
+ * (its reduction), or "ntt_dit_join" with G3H_FUSED_JOIN ("gather" and "small_quotient"
+ * on domains of at most 2^5 points); g3h_ntt "ntt_brev" and "ntt_dit" (or "small_ntt"); a
+ * multiexp its "msm_*" kernels. */
 typedef struct {
   const char* name;
   uint32_t launches;
