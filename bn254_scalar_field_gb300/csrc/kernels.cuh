@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint32_t* __restrict_
     const uint32_t r0 = blockIdx.x * blockDim.x;
     if (r0 < n_rows) {
       const uint32_t r1 = min(n_rows, r0 + blockDim.x);
-      const uint32_t t0 = rp[r0], t1 = min(rp[r1], t0 + (1u << 20));
+      const uint32_t t0 = rp[r0], t1 = t0 + min(rp[r1] - t0, 1u << 20);
       l2_prefetch(val + t0, (t1 - t0) * 32u);
       const uint32_t c0 = t0 & ~3u, c1 = t1 & ~3u;
       l2_prefetch(col + c0, (c1 - c0) * 4u);
