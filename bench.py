@@ -139,7 +139,8 @@ def plan_for(k):
 
 def kernel_counts_per_h(k, nnz_a, nnz_b, from_witness=True):
     """The method's Montgomery multiplies and reductions (from_mont) of one whole H on 2^k
-    (SURVEY's count), charged to the kernel that does them, as {name: (multiplies,
+    (the method's multiply count: every multiply of the algorithm, skipped or not), charged
+    to the kernel that does them, as {name: (multiplies,
     reductions)}. gather_a / gather_b: one multiply per term of A / of B; ntt_dif: the
     butterflies of the inverse's top slice levels (3 vectors) and, from a witness, the n
     products c = a * b formed at its load; ntt_mid: the low levels of both transforms, the
@@ -188,7 +189,7 @@ def algorithmic_ops(kernel, k, nnz_a, nnz_b, from_witness=True):
 
 
 def h_ops(k, nnz_a, nnz_b, from_witness=True):
-    """Algorithmic IMAD results of one whole H on 2^k, SURVEY's count: 6 (n/2) k + 7n
+    """Algorithmic IMAD results of one whole H on 2^k, the method's count: 6 (n/2) k + 7n
     multiplies (butterflies, 1/n, shift, join), with a witness nnz_A + nnz_B + n more (the
     gather and c = a * b), and n reductions."""
     n = 1 << k

@@ -54,12 +54,12 @@ def test_per_kernel_work_sums_to_the_whole_h():
 
 
 def test_h_ops_is_the_multiply_count_of_the_method():
-    # SURVEY's count at 2^18: 6 (n/2) k butterflies + 3n (1/n) + 3n (shift) + n (join)
+    # The method's count at 2^18: 6 (n/2) k butterflies + 3n (1/n) + 3n (shift) + n (join)
     # + nnz_A + nnz_B + n (gather, c = a * b) multiplies, n reductions.
     bench = _bench()
     n, k, nnz_a, nnz_b = 1 << 18, 18, 296223, 443023
     mm = 6 * (n // 2) * k + 3 * n + 3 * n + n + nnz_a + nnz_b + n
-    assert mm == 16992174  # 16.99 M, as SURVEY states
+    assert mm == 16992174  # 16.99 M multiplies
     assert bench.h_ops(k, nnz_a, nnz_b) == mm * (2 * 128 + 8) + n * (2 * 64 + 8)
     # each gather launch is charged its own matrix only
     assert bench.algorithmic_ops("gather_a", k, nnz_a, nnz_b) == nnz_a * 264
