@@ -139,9 +139,9 @@ def plan_for(k):
 
 def kernel_counts_per_h(k, nnz_a, nnz_b, from_witness=True):
     """The method's Montgomery multiplies and reductions (from_mont) of one whole H on 2^k
-    (the method's multiply count: every multiply of the algorithm, skipped or not), charged
-    to the kernel that does them, as {name: (multiplies,
-    reductions)}. gather_a / gather_b: one multiply per term of A / of B; ntt_dif: the
+    (every multiply of the algorithm, skipped by the kernels or not), charged to the kernel
+    that does them, as {name: (multiplies, reductions)}. gather_a / gather_b: one multiply
+    per term of A / of B; ntt_dif: the
     butterflies of the inverse's top slice levels (3 vectors) and, from a witness, the n
     products c = a * b formed at its load; ntt_mid: the low levels of both transforms, the
     1/n scale and the coset shift (3 vectors); ntt_dit: the forward's top levels; prejoin:
