@@ -609,19 +609,21 @@ int quotient_vectors(g3h_ctx* c, const Lane& ln, const cudaStream_t* vs, bool se
   int rc = G3H_OK;
   if (w) {
     // a and b by the gather, A on the stream of a, B on the stream of b; c = a * b is
-    // formed by c's first inverse kernel at its load, once both are done
+    // formed by c's first inverse kernel at its load, once both are done. B's gather (the
+    // longer rows) is issued first, so its blocks take the SMs first: 2^18 H 0.2771 ->
+    // 0.2755 ms against A's first
     NvtxRange range("g3h gather");
     fr_t* ab = ln.ab_in;
     const uint32_t nn = (uint32_t)n;
-    rc = run_on(c, vs[0], "gather_a", [&] {
-      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(
-          c->d_rpa, c->d_cola, c->d_vala, w, c->n_rows_a, nn, c->n_wires, ab, check, c->d_err,
-          0, 0);
+    rc = run_on(c, vs[1], "gather_b", [&] {
+      k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
+          c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, c->n_wires, ab + n, check,
+          c->d_err, 0, 0);
     });
     if (rc == G3H_OK)
-      rc = run_on(c, vs[1], "gather_b", [&] {
-        k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[1]>>>(
-            c->d_rpb, c->d_colb, c->d_valb, w, c->n_rows_b, nn, c->n_wires, ab + n, check,
+      rc = run_on(c, vs[0], "gather_a", [&] {
+        k_gather_rows<<<blocks_for(n, 256), 256, 0, vs[0]>>>(
+            c->d_rpa, c->d_cola, c->d_vala, w, c->n_rows_a, nn, c->n_wires, ab, check,
             c->d_err, 0, 0);
       });
     if (rc != G3H_OK) return rc;
